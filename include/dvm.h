@@ -1,0 +1,177 @@
+/*
+ * dvm.h — C ABI of the DVM hot path on GB300 (sm_103a).
+ *
+ * DVM ("DVM: A Bytecode Virtual Machine Approach for Dynamic Tensor Computation",
+ * review page on the xllm-io paper-review blog, and the MindSpore DVM summary) turns
+ * each dynamic op instance into tile-level bytecode on the CPU and runs it on the
+ * accelerator with an interpreter kernel that is already resident, so that no kernel
+ * is generated or loaded per shape (MindSpore summary, section 3.2 layer 3 and the
+ * comparison table of section 3.4).
+ *
+ * The three calls of the method:
+ *   dvm_graph_add  — streaming fusion: ops arrive one by one and are grouped by the
+ *                    elemwise-elemwise, reduce-forward and matmul+elemwise patterns
+ *                    until a flush (review page section 5.2, "dynamic graph fusion",
+ *                    steps 1–4; MindSpore summary section 3.3).
+ *   dvm_encode     — shape tiling (dominant shape S_d, outer-to-inner shrink,
+ *                    hardware_align_div, cost-model pruning; review page section 4.2)
+ *                    and bytecode encoding (code header with block_dim, body_tile and
+ *                    kernel type, code body with auto-inserted syncs; section 4.3;
+ *                    instructions of Table 1, section 4.1).
+ *   dvm_run        — one launch of the persistent interpreter, grid = SM count,
+ *                    each CTA running its contiguous tile range (section 4.4).
+ *
+ * Conventions for every call:
+ *   - Return value: DVM_OK (0) or a negative dvm_status. No exception crosses the ABI.
+ *     dvm_last_error() gives a one-line reason for the last failure on the context.
+ *   - A dvm_ctx is not thread-safe; use one per host thread.
+ *   - Device memory is always owned by the caller (e.g. a torch tensor's data_ptr()).
+ *     The context owns its graph state and a small device scratch area (grid-barrier
+ *     counter and per-CTA partial sums) allocated by dvm_create.
+ *   - Shapes are int64 extents, row-major; strides are in elements.
+ *   - There is no CPU fallback: every op of the path runs in this library's kernels.
+ */
+#ifndef DVM_H_
+#define DVM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dvm_ctx dvm_ctx;
+typedef int32_t dvm_status;
+
+/* status codes */
+enum {
+  DVM_OK = 0,
+  DVM_E_INVALID_ARG = -1,    /* null pointer, bad id, bad rank, misaligned pointer */
+  DVM_E_UNSUPPORTED_OP = -2, /* op or pattern the fuser/encoder does not handle */
+  DVM_E_SHAPE = -3,          /* given output shape differs from the inferred one */
+  DVM_E_BUF_TOO_SMALL = -4,  /* dvm_encode: cap too small (needed length in *len) */
+  DVM_E_BYTECODE = -5,       /* dvm_run / dvm_validate: malformed launch image */
+  DVM_E_CUDA = -6,           /* a CUDA runtime call failed */
+  DVM_E_STATE = -7,          /* call out of order (e.g. encode before flush) */
+  DVM_E_CAPACITY = -8,       /* no feasible tiling / too many tensors or instructions */
+  /* device-side status words, read back with dvm_poll_status */
+  DVM_E_TIMEOUT = -100,      /* a bounded wait (grid barrier, mbarrier) gave up */
+  DVM_E_BAD_OPCODE = -101,   /* the interpreter met an opcode it does not know */
+  DVM_E_BOUNDS = -102        /* a slot or tensor index out of range */
+};
+
+/* element types; compute is fp32 in registers */
+typedef enum { DVM_F32 = 1, DVM_BF16 = 2, DVM_U8 = 3 } dvm_dtype;
+
+/* graph ops (value semantics: every op is computed as if alone, then rounded to its
+ * output dtype; fusion keeps intermediates in registers) */
+typedef enum {
+  DVM_OP_COPY = 1, DVM_OP_SQRT = 2, DVM_OP_ABS = 3, DVM_OP_LOG = 4, DVM_OP_EXP = 5,
+  DVM_OP_ROUND = 6,      /* half to even */
+  DVM_OP_FLOOR = 7,
+  DVM_OP_ISFINITE = 8,   /* output dtype must be DVM_U8 (0/1) */
+  DVM_OP_NEG = 9, DVM_OP_RSQRT = 10, DVM_OP_RECIP = 11,
+  DVM_OP_SILU = 12,      /* x / (1 + exp(-x)) */
+  DVM_OP_CAST = 13,      /* to F32 or BF16 */
+  DVM_OP_BROADCAST = 14, /* to the given shape */
+  /* two tensor inputs, numpy broadcasting */
+  DVM_OP_ADD = 20, DVM_OP_SUB = 21, DVM_OP_MUL = 22, DVM_OP_DIV = 23,
+  DVM_OP_MAX = 24, DVM_OP_MIN = 25, /* NaN-propagating */
+  DVM_OP_POW = 26,                  /* C99 powf */
+  /* one tensor input and a float scalar attrs[0]; attrs[1] != 0 puts the scalar on
+   * the left (s - x, s / x, s ** x) */
+  DVM_OP_ADDS = 30, DVM_OP_SUBS = 31, DVM_OP_MULS = 32, DVM_OP_DIVS = 33,
+  DVM_OP_MAXS = 34, DVM_OP_MINS = 35, DVM_OP_POWS = 36,
+  /* reductions over the last axis, keepdim */
+  DVM_OP_REDUCE_SUM = 40, DVM_OP_REDUCE_MAX = 41, DVM_OP_REDUCE_MEAN = 42,
+  DVM_OP_REDUCE_SUM_ALL = 43, /* over every element, shape [1] */
+  DVM_OP_SELECT_GT0 = 50,     /* inputs (p, a, b): a if the scalar p > 0 else b */
+  DVM_OP_MATMUL = 60,         /* A[M,K] x W[K,N], bf16, W with stride 1 along K */
+  DVM_OP_OPAQUE = 70          /* an op DVM does not run: closes the open group; the
+                                 caller then calls dvm_flush and runs the launches */
+} dvm_op;
+
+/* description of the device the encoder plans for (see dvm_create_host) */
+typedef struct {
+  int32_t num_cores;      /* CTAs per launch; default: SM count */
+  int32_t cap_elems;      /* padded elements per tile; default 8192 */
+  int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 196608 */
+  int32_t max_stages;     /* default 8 */
+  int32_t c0_bytes;       /* per-tile overhead of the cost model; default 4096 */
+  int32_t flops_per_byte; /* cube cost-model balance; default 280 */
+  int32_t n_slots;        /* register slots besides ACC; must be 4 */
+} dvm_device_desc;
+
+/* counters (MindSpore summary section 3.2 flush reasons; encode latency) */
+typedef struct {
+  int64_t ops_added;
+  int64_t groups_closed;
+  int64_t flushes;
+  int64_t launches_encoded;
+  int64_t programs_encoded;
+  int64_t runs;
+  int64_t host_ns_total;   /* time spent inside graph_add/flush/encode */
+  int64_t host_ns_last;    /* same, since the last dvm_reset or dvm_stats_reset */
+} dvm_stats_t;
+
+/* Create a context bound to CUDA device `cuda_device` (queries the SM count; allocates
+ * 256 bytes of device scratch). */
+dvm_status dvm_create(dvm_ctx** out, int cuda_device);
+/* Create an encode-only context for `desc` (no CUDA calls; dvm_run refuses). NULL desc
+ * = defaults with num_cores 152. */
+dvm_status dvm_create_host(dvm_ctx** out, const dvm_device_desc* desc);
+void dvm_destroy(dvm_ctx* ctx);
+/* Drop all values, ops and groups; value ids restart at 0. */
+dvm_status dvm_reset(dvm_ctx* ctx);
+dvm_status dvm_get_desc(const dvm_ctx* ctx, dvm_device_desc* out);
+
+/* Declare an external tensor (an input, or the output of an op DVM did not run).
+ * strides == NULL means contiguous. rank 1..4. */
+dvm_status dvm_input(dvm_ctx* ctx, dvm_dtype dtype, int rank, const int64_t* shape,
+                     const int64_t* strides, int32_t* out_id);
+/* Append one op to the stream. `shape`/`rank` is the result shape (checked against
+ * the inferred one; for DVM_OP_OPAQUE it is taken as given, rank 0 = no result).
+ * `attrs` holds the scalar attributes of the scalar-form ops. *out_id = result value
+ * id (-1 for an opaque op without result). */
+dvm_status dvm_graph_add(dvm_ctx* ctx, dvm_op op, const int32_t* inputs, int n_inputs,
+                         const int64_t* shape, int rank, dvm_dtype out_dtype,
+                         const float* attrs, int n_attrs, int32_t* out_id);
+/* Ask that value `id` be written to memory (otherwise a fused intermediate lives only
+ * in registers unless an op of another group reads it). */
+dvm_status dvm_mark_output(dvm_ctx* ctx, int32_t id);
+/* Query a value: dtype, rank, shape[4]. */
+dvm_status dvm_value_info(const dvm_ctx* ctx, int32_t id, int32_t* dtype, int32_t* rank,
+                          int64_t* shape);
+/* Close the open group and turn the pending groups into launches (independent
+ * element-wise groups are stacked into one launch). *n_launches = launches to encode. */
+dvm_status dvm_flush(dvm_ctx* ctx, int32_t* n_launches);
+/* Write the launch image of launch `launch` (0..n_launches-1 of the last flush) into
+ * buf[0..cap). *len = bytes written (or needed, with DVM_E_BUF_TOO_SMALL).
+ * tensor_ids[0..*n_tensors) = value ids in binding order (capacity 16). */
+dvm_status dvm_encode(dvm_ctx* ctx, int32_t launch, uint8_t* buf, size_t cap, size_t* len,
+                      int32_t* tensor_ids, int32_t* n_tensors);
+/* Check a launch image (header, offsets, opcodes, slot/tensor/jump ranges). */
+dvm_status dvm_validate(const uint8_t* image, size_t len);
+/* Launch the interpreter for one image on `stream` (a cudaStream_t; NULL = legacy
+ * default stream). tensor_ptrs are device pointers in binding order, each 16-byte
+ * aligned. The image is copied into the kernel parameters, so `image` may be reused
+ * as soon as the call returns. Asynchronous. */
+dvm_status dvm_run(dvm_ctx* ctx, const uint8_t* image, size_t len, void* const* tensor_ptrs,
+                   int n_tensors, void* stream);
+/* Synchronise `stream` and read the device status word (0 or a DVM_E_* device code).
+ * A non-zero word is cleared and the grid-barrier state is re-initialised. */
+dvm_status dvm_poll_status(dvm_ctx* ctx, void* stream, int32_t* device_status);
+const char* dvm_last_error(const dvm_ctx* ctx);
+dvm_status dvm_stats(const dvm_ctx* ctx, dvm_stats_t* out);
+dvm_status dvm_stats_reset_last(dvm_ctx* ctx);
+
+/* Test hook: make the next grid barrier of `ctx` skip one CTA's arrival so that the
+ * bounded wait expires (checks the timeout path; never hangs: the wait is limited to
+ * about `timeout_ms` milliseconds). timeout_ms <= 0 restores the default (2000). */
+dvm_status dvm_debug_set_barrier(dvm_ctx* ctx, int skip_one_arrival, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DVM_H_ */

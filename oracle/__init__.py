@@ -1,0 +1,29 @@
+"""Oracle for the DVM hot path: TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, CPU-only statement of what the fused tile
+programs compute, written from the DVM review page ("DVM: A Bytecode Virtual
+Machine Approach for Dynamic Tensor Computation", xllm-io paper-review blog)
+and the MindSpore DVM summary page.  It shares no code with the CUDA path
+(`bytecode_vm_jit_gb300/csrc`): no kernels, headers, constants or helpers.
+
+Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s CPU-baseline leg may
+import it.  The product path never routes through it; there is no CPU
+fallback.
+
+Modules
+-------
+bf16         fp64 -> bfloat16 round-to-nearest-even (used to model bf16
+             materialisation of an op's result).
+evaluator    op-graph evaluator: every op in fp64 on the exact input values,
+             rounded once to the op's declared output dtype.  No bytecode, no
+             fusion, no tiling.
+ref_encoder  reference streaming fuser + shape tiler + bytecode encoder,
+             written from the bytecode specification in the design notes;
+             its bytes must equal the C++ encoder's bit for bit.
+make_golden  script that writes tests/golden/*.txt using only this package.
+
+Parity status: every function here is pinned by `-m "not gpu"` tests in
+tests/test_oracle_*.py and tests/test_ref_encoder.py (closed forms,
+invariants, brute force, library special cases).  No function is
+"parity unpinned".
+"""

@@ -1,0 +1,979 @@
+"""Reference streaming fuser, shape tiler and bytecode encoder (test infrastructure).
+
+Written from the bytecode specification in the design notes (sections "Streaming
+fuser", "Views", "Tiling", "Load flags", "Lowering", "Instruction word", "Launch
+image"), which restate the DVM review page: dynamic-graph streaming fusion (section
+5.2, steps 1-4), shape tiling with a dominant shape, outer-to-inner shrink,
+hardware_align_div and cost-model pruning (section 4.2), the code header/body format
+with auto-inserted syncs (section 4.3) and the tile-level virtual instructions of
+Table 1 (section 4.1).
+
+Plain Python, no numpy in the arithmetic, clarity over speed.  It must produce the
+same bytes as the C++ library for every op stream and device description; the tests
+compare the two.
+"""
+import struct
+
+# ---------------------------------------------------------------- constants --
+F32, BF16, U8 = 1, 2, 3
+ESZ = {F32: 4, BF16: 2, U8: 1}
+
+OPS = {
+    "copy": 1, "sqrt": 2, "abs": 3, "log": 4, "exp": 5, "round": 6, "floor": 7,
+    "isfinite": 8, "neg": 9, "rsqrt": 10, "recip": 11, "silu": 12, "cast": 13,
+    "broadcast": 14,
+    "add": 20, "sub": 21, "mul": 22, "div": 23, "max": 24, "min": 25, "pow": 26,
+    "adds": 30, "subs": 31, "muls": 32, "divs": 33, "maxs": 34, "mins": 35, "pows": 36,
+    "reduce_sum": 40, "reduce_max": 41, "reduce_mean": 42, "reduce_sum_all": 43,
+    "select_gt0": 50, "matmul": 60, "opaque": 70,
+}
+UNARY_CODES = {1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14}
+BINARY_CODES = {20, 21, 22, 23, 24, 25, 26}
+SCALAR_CODES = {30, 31, 32, 33, 34, 35, 36}
+RRED_CODES = {40, 41, 42}
+
+# VM opcodes
+I_LD, I_ST, I_MOV, I_BCAST, I_WAIT, I_REL = 0x01, 0x02, 0x03, 0x04, 0x05, 0x06
+UNARY_VM = {2: 0x10, 3: 0x11, 4: 0x12, 5: 0x13, 6: 0x14, 7: 0x15, 8: 0x16,
+            9: 0x17, 10: 0x18, 11: 0x19, 12: 0x1A}
+I_CASTBF = 0x1B
+BIN_VM = {20: 0x20, 21: 0x21, 22: 0x22, 23: 0x23, 24: 0x24, 25: 0x25, 26: 0x26}
+I_RSUM, I_RMAX, I_ASUM = 0x30, 0x31, 0x32
+I_TILES, I_GSUM, I_JLE0, I_JMP, I_SST, I_END = 0x40, 0x41, 0x42, 0x43, 0x44, 0x45
+I_MMA = 0x50
+
+# LD flags
+L_DMA, L_HOIST, L_COLV, L_ROWV, L_FIRST = 1, 2, 4, 8, 16
+# compute flags
+K_AROW, K_XROW, K_REV, K_IMM = 1, 2, 4, 8
+
+VEC, SEC, CUBE = 0, 1, 2
+KT_VEC, KT_CUBE = 1, 2
+MAGIC = 0x314D5644
+MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
+
+DEFAULT_DESC = dict(num_cores=152, cap_elems=8192, smem_budget=196608, max_stages=8,
+                    c0_bytes=4096, flops_per_byte=280, n_slots=4)
+
+
+class EncodeError(Exception):
+    pass
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def round_up(a, b):
+    return cdiv(a, b) * b
+
+
+def hardware_align_div(n, k, al):
+    """Tile extent: ceil(n/k) rounded up to a multiple of the instruction width al."""
+    return round_up(cdiv(n, k), al)
+
+
+def f32_bits(x):
+    return struct.unpack("<I", struct.pack("<f", x))[0]
+
+
+def op_class(code):
+    if code in UNARY_CODES or code in BINARY_CODES or code in SCALAR_CODES:
+        return "ELT"
+    if code in RRED_CODES:
+        return "RRED"
+    return {43: "ARED", 50: "SEL", 60: "MM", 70: "OPQ"}[code]
+
+
+def contiguous_strides(shape):
+    st, acc = [], 1
+    for e in reversed(shape):
+        st.append(acc)
+        acc *= e
+    return list(reversed(st))
+
+
+def broadcast_shapes(a, b):
+    r = max(len(a), len(b))
+    a = [1] * (r - len(a)) + list(a)
+    b = [1] * (r - len(b)) + list(b)
+    out = []
+    for x, y in zip(a, b):
+        if x == y or y == 1:
+            out.append(x)
+        elif x == 1:
+            out.append(y)
+        else:
+            raise EncodeError("shape")
+    return out
+
+
+# ------------------------------------------------------------------- graph --
+class Value:
+    def __init__(self, vid, dtype, shape, strides, producer):
+        self.id, self.dtype, self.shape = vid, dtype, list(shape)
+        self.strides = list(strides)
+        self.producer = producer          # op index or None
+        self.group = None                 # group index for op results
+        self.output = False
+        self.consumers = []               # op indices
+
+
+class Op:
+    def __init__(self, code, inputs, out, dtype, attrs, shape):
+        self.code, self.inputs, self.out = code, list(inputs), out
+        self.dtype, self.attrs, self.shape = dtype, list(attrs), list(shape)
+        self.cls = op_class(code)
+
+
+class Group:
+    def __init__(self, kind, G):
+        self.kind, self.G = kind, list(G)
+        self.ops = []
+        self.ared = None      # value id of the grid-wide sum
+        self.ared_pos = -1    # index in ops
+        self.sel = None       # op index
+        self.has_rred = False
+
+
+def iter_shape(ctx, op):
+    if op.cls in ("RRED", "ARED"):
+        return ctx.values[op.inputs[0]].shape
+    return op.shape
+
+
+def rowshape(G):
+    return list(G[:-1]) + [1]
+
+
+def view_strides(val_shape, val_strides, G):
+    r, q = len(G), len(val_shape)
+    if q > r:
+        raise EncodeError("shape")
+    vs = []
+    for d in range(r):
+        j = d - (r - q)
+        if j < 0 or val_shape[j] == 1:
+            vs.append(0)
+        elif val_shape[j] == G[d]:
+            vs.append(val_strides[j])
+        else:
+            raise EncodeError("shape")
+    return vs
+
+
+# ---------------------------------------------------------------- lowering --
+class Lowering:
+    """Accumulator-machine lowering of one section (spec section "Lowering")."""
+
+    def __init__(self, ctx, G, ops, stored, n_slots, store_as=None):
+        self.ctx, self.G, self.ops = ctx, G, ops
+        self.stored = stored            # set of value ids to store
+        self.store_as = store_as or {}  # value id -> tensor value id to store into
+        self.n_slots = n_slots
+        self.body = []                  # list of dicts
+        self.acc = None
+        self.slot = {}
+        self.free = list(range(1, n_slots + 1))
+        self.rem = {}
+        self.kind = {}
+        for op in ops:
+            if op.cls == "MM":
+                continue
+            for v in op.inputs:
+                self.rem[v] = self.rem.get(v, 0) + 1
+        self.group_vals = set(op.out for op in ops)
+
+    def value_kind(self, v):
+        if v in self.kind:
+            return self.kind[v]
+        val = self.ctx.values[v]
+        vs = view_strides(val.shape, val.strides, self.G)
+        return "ROW" if vs[-1] == 0 else "FULL"
+
+    def is_external(self, v):
+        return v not in self.group_vals
+
+    def alloc(self):
+        if not self.free:
+            raise EncodeError("slots")
+        self.free.sort()
+        return self.free.pop(0)
+
+    def emit(self, op, a=0, b=0, flags=0, imm=0, tensor=None):
+        self.body.append(dict(op=op, a=a, b=b, flags=flags, imm=imm, aux0=0, tensor=tensor))
+
+    def load(self, v, dst):
+        self.emit(I_LD, a=dst, tensor=v)
+
+    def to_acc(self, v):
+        if self.acc == v:
+            return
+        if v in self.slot:
+            self.emit(I_MOV, a=0, b=self.slot[v], flags=1 if self.value_kind(v) == "ROW" else 0)
+        elif self.is_external(v):
+            if self.rem[v] == 1:
+                self.load(v, 0)
+            else:
+                k = self.alloc()
+                self.load(v, k)
+                self.slot[v] = k
+                self.emit(I_MOV, a=0, b=k, flags=1 if self.value_kind(v) == "ROW" else 0)
+        else:
+            raise EncodeError("lost value")
+        self.acc = v
+
+    def operand_slot(self, v):
+        if v in self.slot:
+            return self.slot[v]
+        k = self.alloc()
+        if self.is_external(v):
+            self.load(v, k)
+        elif self.acc == v:
+            self.emit(I_MOV, a=k, b=0, flags=1 if self.value_kind(v) == "ROW" else 0)
+        else:
+            raise EncodeError("lost value")
+        self.slot[v] = k
+        return k
+
+    def run(self):
+        ctx = self.ctx
+        n = len(self.ops)
+        for i, op in enumerate(self.ops):
+            code = op.code
+            r = op.out
+            if op.cls == "MM":
+                self.body.append(dict(op=I_MMA, a=0, b=0, flags=0, imm=0, aux0=0, tensor=None,
+                                      ta=op.inputs[0], tb=op.inputs[1]))
+                rkind = "FULL"
+            elif op.cls == "ELT" and code in BINARY_CODES:
+                p, q = op.inputs
+                if self.acc == p and p != q:
+                    x, rev = self.operand_slot(q), 0
+                elif self.acc == q and p != q:
+                    x, rev = self.operand_slot(p), 1
+                elif p == q:
+                    self.to_acc(p)
+                    x, rev = self.operand_slot(p), 0
+                else:
+                    self.to_acc(p)
+                    x, rev = self.operand_slot(q), 0
+                kp, kq = self.value_kind(p), self.value_kind(q)
+                ka = kq if rev else kp     # kind of the value in ACC
+                kx = kp if rev else kq
+                flags = (K_AROW if ka == "ROW" else 0) | (K_XROW if kx == "ROW" else 0) | (K_REV if rev else 0)
+                self.emit(BIN_VM[code], a=x, flags=flags)
+                rkind = "ROW" if (kp == "ROW" and kq == "ROW") else "FULL"
+            else:
+                p = op.inputs[0]
+                self.to_acc(p)
+                kp = self.value_kind(p)
+                af = K_AROW if kp == "ROW" else 0
+                rkind = kp
+                if code in SCALAR_CODES:
+                    left = len(op.attrs) > 1 and op.attrs[1] != 0
+                    self.emit(BIN_VM[code - 10], flags=af | K_IMM | (K_REV if left else 0),
+                              imm=f32_bits(op.attrs[0]))
+                elif code in UNARY_VM:
+                    self.emit(UNARY_VM[code], flags=af)
+                elif code in (1, 13):       # copy, cast
+                    pass
+                elif code == 14:            # broadcast
+                    if kp == "ROW" and op.shape[-1] != 1:
+                        self.emit(I_BCAST)
+                        rkind = "FULL"
+                elif code in RRED_CODES:
+                    if kp == "FULL":
+                        self.emit(I_RMAX if code == 41 else I_RSUM)
+                        if code == 42:
+                            nin = ctx.values[p].shape[-1]
+                            self.emit(BIN_VM[23], flags=K_AROW | K_IMM, imm=f32_bits(float(nin)))
+                    rkind = "ROW"
+                elif code == 43:
+                    self.emit(I_ASUM, flags=af)
+                    rkind = "ROW"
+                else:
+                    raise EncodeError("op in body")
+            self.acc = r
+            self.kind[r] = rkind
+            if code != 43:
+                if op.dtype == BF16:
+                    self.emit(I_CASTBF, flags=K_AROW if rkind == "ROW" else 0)
+                if r in self.stored:
+                    self.emit(I_ST, tensor=r, flags=L_ROWV if rkind == "ROW" else 0)
+                if r in self.store_as:
+                    self.emit(I_ST, tensor=self.store_as[r], flags=L_ROWV if rkind == "ROW" else 0)
+            for v in (set(op.inputs) if op.cls != "MM" else ()):
+                self.rem[v] -= op.inputs.count(v)
+                if self.rem[v] == 0 and v in self.slot:
+                    self.free.append(self.slot.pop(v))
+            if code == 43:
+                continue
+            rr = self.rem.get(r, 0)
+            nxt_reads = i + 1 < n and r in self.ops[i + 1].inputs
+            if rr >= 2 or (rr == 1 and not nxt_reads):
+                k = self.alloc()
+                self.emit(I_MOV, a=k, b=0, flags=1 if rkind == "ROW" else 0)
+                self.slot[r] = k
+        if len(self.body) > MAX_INSTR - 2:
+            raise EncodeError("too many instructions")
+        return self.body
+
+
+# --------------------------------------------------------------------- ctx --
+class RefCtx:
+    def __init__(self, desc=None):
+        self.desc = dict(DEFAULT_DESC)
+        if desc:
+            self.desc.update(desc)
+        self.reset()
+
+    def reset(self):
+        self.values, self.ops, self.groups = [], [], []
+        self.open = None
+        self.pending = []
+        self.launches = []
+
+    # -- graph building
+    def input(self, dtype, shape, strides=None):
+        v = Value(len(self.values), dtype, shape, strides or contiguous_strides(shape), None)
+        self.values.append(v)
+        return v.id
+
+    def infer_shape(self, code, ins, shape):
+        V = self.values
+        cls = op_class(code)
+        if cls == "ELT":
+            if code in BINARY_CODES:
+                return broadcast_shapes(V[ins[0]].shape, V[ins[1]].shape)
+            if code == 14:
+                broadcast_shapes(V[ins[0]].shape, shape)
+                return list(shape)
+            return list(V[ins[0]].shape)
+        if cls == "RRED":
+            return list(V[ins[0]].shape[:-1]) + [1]
+        if cls == "ARED":
+            return [1]
+        if cls == "SEL":
+            p = V[ins[0]]
+            n = 1
+            for e in p.shape:
+                n *= e
+            if n != 1:
+                raise EncodeError("shape")
+            return broadcast_shapes(V[ins[1]].shape, V[ins[2]].shape)
+        if cls == "MM":
+            a, w = V[ins[0]].shape, V[ins[1]].shape
+            if len(a) != 2 or len(w) != 2 or a[1] != w[0]:
+                raise EncodeError("shape")
+            return [a[0], w[1]]
+        return list(shape)
+
+    def graph_add(self, name, ins, shape, dtype, attrs=()):
+        code = OPS[name] if isinstance(name, str) else name
+        cls = op_class(code)
+        if cls == "OPQ":
+            self.close_open()
+            if len(shape) == 0:
+                return -1
+            return self.input(dtype, shape)
+        shp = self.infer_shape(code, ins, shape)
+        if list(shape) != shp:
+            raise EncodeError("shape")
+        if code == 8 and dtype != U8:
+            raise EncodeError("unsupported")
+        if dtype == U8 and code != 8:
+            raise EncodeError("unsupported")
+        v = Value(len(self.values), dtype, shp, contiguous_strides(shp), len(self.ops))
+        self.values.append(v)
+        op = Op(code, ins, v.id, dtype, attrs, shp)
+        self.ops.append(op)
+        oi = len(self.ops) - 1
+        for u in ins:
+            self.values[u].consumers.append(oi)
+        if cls == "MM":
+            self.close_open()
+            self.start_group(CUBE, shp, oi)
+        elif self.open is not None and self.accepts(self.open, oi):
+            self.append(self.open, oi)
+        else:
+            self.close_open()
+            if cls == "SEL":
+                raise EncodeError("unsupported")
+            kind = SEC if cls == "ARED" else VEC
+            G = iter_shape(self, op)
+            if cls == "RRED" and not self.row_fits(G, [self.values[ins[0]].dtype, dtype]):
+                raise EncodeError("unsupported")
+            self.start_group(kind, G, oi)
+        return v.id
+
+    def start_group(self, kind, G, oi):
+        g = Group(kind, G)
+        self.groups.append(g)
+        self.open = len(self.groups) - 1
+        self.append(self.open, oi)
+
+    def append(self, gi, oi):
+        g = self.groups[gi]
+        op = self.ops[oi]
+        g.ops.append(oi)
+        self.values[op.out].group = gi
+        if op.cls == "RRED":
+            g.has_rred = True
+        if op.cls == "ARED":
+            g.ared, g.ared_pos = op.out, len(g.ops) - 1
+            g.kind = SEC
+        if op.cls == "SEL":
+            g.sel = oi
+
+    def close_open(self):
+        if self.open is not None:
+            self.pending.append(self.open)
+            self.open = None
+
+    def group_dtypes(self, g, extra_op=None):
+        dts = []
+        for oi in g.ops + ([extra_op] if extra_op is not None else []):
+            op = self.ops[oi]
+            dts.append(op.dtype)
+            for u in op.inputs:
+                dts.append(self.values[u].dtype)
+        return dts
+
+    def row_fits(self, G, dtypes):
+        a = 512 // min(ESZ[d] for d in dtypes)
+        return round_up(G[-1], a) <= self.desc["cap_elems"]
+
+    def accepts(self, gi, oi):
+        g = self.groups[gi]
+        op = self.ops[oi]
+        V = self.values
+        isG = iter_shape(self, op)
+        if op.cls in ("MM", "OPQ"):
+            return False
+        if g.kind == CUBE:
+            if op.cls != "ELT" or isG != g.G:
+                return False
+            if any(len(V[u].shape) > 2 for u in op.inputs):
+                return False
+        elif g.kind == VEC:
+            if op.cls == "ELT":
+                if isG != g.G and isG != rowshape(g.G):
+                    return False
+            elif op.cls == "RRED":
+                if isG != g.G:
+                    return False
+                if not self.row_fits(g.G, self.group_dtypes(g, oi)):
+                    return False
+            elif op.cls == "ARED":
+                if isG != g.G or g.has_rred:
+                    return False
+            else:
+                return False
+        else:  # SEC
+            if g.sel is not None:
+                return False
+            pre = set(self.ops[j].out for j in g.ops[:g.ared_pos + 1])
+            if op.cls == "ELT":
+                if isG != g.G:
+                    return False
+                if any(u in pre for u in op.inputs):
+                    return False
+            elif op.cls == "SEL":
+                p, a, b = op.inputs
+                if p != g.ared:
+                    return False
+                post = set(self.ops[j].out for j in g.ops[g.ared_pos + 1:])
+                for u in (a, b):
+                    if u not in post or V[u].shape != g.G or V[u].dtype != op.dtype:
+                        return False
+            else:
+                return False
+        return self.dry_run(g, oi)
+
+    def dry_run(self, g, extra):
+        ops = [self.ops[j] for j in g.ops] + [self.ops[extra]]
+        try:
+            for sec in self.sections(g, ops, dry=True):
+                Lowering(self, g.G, sec[0], set(), self.desc["n_slots"], sec[1]).run()
+        except EncodeError:
+            return False
+        return True
+
+    def sections(self, g, ops, dry=False):
+        """Op lists of the group's sections: [(ops, store_as)]."""
+        if not any(o.cls == "ARED" for o in ops):
+            return [(ops, {})]
+        apos = next(i for i, o in enumerate(ops) if o.cls == "ARED")
+        secA = ops[:apos + 1]
+        post = ops[apos + 1:]
+        sel = [o for o in post if o.cls == "SEL"]
+        if not sel:
+            return [(secA, {}), (post, {})] if post else [(secA, {})]
+        sel = sel[0]
+        body = [o for o in post if o.cls != "SEL"]
+        outs = {}
+        for o in body:
+            outs[o.out] = o
+        res = [(secA, {})]
+        for root in (sel.inputs[1], sel.inputs[2]):
+            need = set()
+            stack = [root]
+            while stack:
+                v = stack.pop()
+                if v in outs and v not in need:
+                    need.add(v)
+                    stack.extend(outs[v].inputs)
+            res.append(([o for o in body if o.out in need], {} if dry else {root: sel.out}))
+        return res
+
+    def mark_output(self, vid):
+        self.values[vid].output = True
+
+    # -- flush: groups -> launches
+    def group_reads(self, gi):
+        g = self.groups[gi]
+        vals = set()
+        for oi in g.ops:
+            for u in self.ops[oi].inputs:
+                if self.values[u].group != gi:
+                    vals.add(u)
+        return vals
+
+    def flush(self):
+        self.close_open()
+        self.plans = {}
+        self.launches = []
+        cur = None
+        for gi in self.pending:
+            if cur is not None and self.can_stack(cur, gi):
+                cur.append(gi)
+            else:
+                if cur is not None:
+                    self.launches.append(cur)
+                cur = [gi]
+        if cur is not None:
+            self.launches.append(cur)
+        self.pending = []
+        return len(self.launches)
+
+    def can_stack(self, launch, gi):
+        g = self.groups[gi]
+        if g.kind != VEC or any(self.groups[x].kind != VEC for x in launch):
+            return False
+        if len(launch) >= MAX_PROGS:
+            return False
+        if self.group_align(gi) != self.group_align(launch[0]):
+            return False
+        reads = self.group_reads(gi)
+        if any(self.values[u].group in launch for u in reads):
+            return False
+        progs = [self.build_program(x) for x in launch + [gi]]
+        binds = []
+        for p in progs:
+            for t in p["tensors"]:
+                if t["vid"] not in binds:
+                    binds.append(t["vid"])
+        if len(binds) > MAX_BIND:
+            return False
+        stage = max(p["stage_bytes"] for p in progs)
+        hoist = sum(p["hoist_bytes"] for p in progs)
+        return 2 * stage + hoist <= self.desc["smem_budget"]
+
+    def stored_values(self, gi):
+        g = self.groups[gi]
+        out = set()
+        for oi in g.ops:
+            v = self.values[self.ops[oi].out]
+            if v.output or any(self.ops[c].out is not None and self.values[self.ops[c].out].group != gi
+                               for c in v.consumers):
+                out.add(v.id)
+        return out
+
+    def program_tensors_dtypes(self, gi):
+        g = self.groups[gi]
+        stored = self.stored_values(gi)
+        dts = []
+        for oi in g.ops:
+            op = self.ops[oi]
+            for u in op.inputs:
+                if self.values[u].group != gi:
+                    dts.append(self.values[u].dtype)
+            if op.out in stored:
+                dts.append(op.dtype)
+            if op.cls == "SEL":
+                dts.append(op.dtype)
+        return dts
+
+    def group_align(self, gi):
+        dts = self.program_tensors_dtypes(gi)
+        return 512 // min(ESZ[d] for d in dts)
+
+    # -- program construction
+    def lower_group(self, gi):
+        g = self.groups[gi]
+        ops = [self.ops[j] for j in g.ops]
+        stored = self.stored_values(gi)
+        ns = self.desc["n_slots"]
+        secs = self.sections(g, ops)
+        if g.kind == SEC:
+            post_vals = set(o.out for o in ops[g.ared_pos + 1:] if o.cls != "SEL")
+            sel_out = self.ops[g.sel].out if g.sel is not None else None
+            bad = [v for v in stored if v in post_vals] if g.sel is not None else []
+            if bad:
+                raise EncodeError("unsupported: branch value used outside the select")
+        bodies = []
+        for sops, store_as in secs:
+            st = set(v for v in stored if v != g.ared)
+            bodies.append(Lowering(self, g.G, sops, st, ns, store_as).run())
+        return bodies
+
+    def build_program(self, gi):
+        if gi in getattr(self, "plans", {}):
+            return self.plans[gi]
+        g = self.groups[gi]
+        bodies = self.lower_group(gi)
+        # tensor table in order of first reference
+        tensors, index = [], {}
+
+        def ref(v):
+            if v not in index:
+                index[v] = len(tensors)
+                val = self.values[v]
+                tensors.append(dict(vid=v, dtype=val.dtype))
+            return index[v]
+
+        for body in bodies:
+            for ins in body:
+                if ins["op"] == I_MMA:
+                    ins["a"], ins["b"] = ref(ins["ta"]), ref(ins["tb"])
+                elif ins["tensor"] is not None:
+                    t = ref(ins["tensor"])
+                    if ins["op"] == I_LD:
+                        ins["b"] = t
+                    else:
+                        ins["a"] = t
+        sst = None
+        if g.kind == SEC and g.ared in self.stored_values(gi):
+            sst = ref(g.ared)
+        if len(tensors) > MAX_TENS:
+            raise EncodeError("too many tensors")
+        min_esz = min(ESZ[t["dtype"]] for t in tensors)
+        a = 512 // min_esz
+        G = list(g.G)
+        r = len(G)
+        mm_operands = set()
+        if g.kind == CUBE:
+            mm = self.ops[g.ops[0]]
+            mm_operands = {mm.inputs[0], mm.inputs[1]}
+        for t in tensors:
+            val = self.values[t["vid"]]
+            if t["vid"] in mm_operands:
+                t["vs"] = list(val.strides) + [0] * (r - len(val.strides))
+            else:
+                t["vs"] = view_strides(val.shape, val.strides, G)
+        prog = dict(gi=gi, kind=g.kind, G=G, rank=r, a=a, tensors=tensors, bodies=bodies, sst=sst)
+        if g.kind == CUBE:
+            self.plan_cube(prog)
+        else:
+            self.plan_vec(prog, g.has_rred)
+        self.plans[gi] = prog
+        return prog
+
+    # -- tiling
+    def flags_for(self, prog, t, tiles):
+        """LD flags, region sizes and the stage/hoist byte totals for plan t."""
+        G, r = prog["G"], prog["rank"]
+        rows = 1
+        for d in range(r - 1):
+            rows *= t[d]
+        res = {}
+        for ti, ten in enumerate(prog["tensors"]):
+            vs = ten["vs"]
+            esz = ESZ[ten["dtype"]]
+            rowv = vs[r - 1] == 0
+            dma = (not rowv and vs[r - 1] == 1 and (G[r - 1] * esz) % 16 == 0 and
+                   all((vs[d] * esz) % 16 == 0 for d in range(r - 1)))
+            hoist = all(vs[d] == 0 for d in range(r) if tiles[d] > 1)
+            colv = all(vs[d] == 0 for d in range(r - 1) if t[d] > 1)
+            size = round_up((1 if colv else rows) * t[r - 1] * esz, 128)
+            res[ti] = dict(dma=dma, hoist=hoist, colv=colv, rowv=rowv, size=size)
+        return res, rows
+
+    def layout(self, prog, fl):
+        """Assign stage / hoist offsets; returns (stage_bytes, hoist_bytes, per-section offsets)."""
+        stage_max = 0
+        hoist = 0
+        hoff = {}
+        soffs = []
+        for body in prog["bodies"]:
+            off = 0
+            so = {}
+            for ins in body:
+                if ins["op"] != I_LD:
+                    continue
+                ti = ins["b"]
+                f = fl[ti]
+                if not f["dma"]:
+                    continue
+                if f["hoist"]:
+                    if ti not in hoff:
+                        hoff[ti] = hoist
+                        hoist += f["size"]
+                elif ti not in so:
+                    so[ti] = off
+                    off += f["size"]
+            stage_max = max(stage_max, off)
+            soffs.append(so)
+        return stage_max, hoist, soffs, hoff
+
+    def plan_vec(self, prog, rowred):
+        d_ = self.desc
+        G, r, a = prog["G"], prog["rank"], prog["a"]
+        al = [1] * (r - 1) + [a]
+        t = list(G[:r - 1]) + [hardware_align_div(G[r - 1], 1, a)]
+        cands = [list(t)]
+        for d in range(r):
+            if d == r - 1 and rowred:
+                break
+            k = 2
+            while True:
+                c = cdiv(G[d], k)
+                nt = round_up(c, al[d])
+                if nt < t[d]:
+                    t[d] = nt
+                    cands.append(list(t))
+                if c <= 1 or nt <= al[d]:
+                    break
+                k *= 2
+        best = None
+        for cand in cands:
+            tiles = [cdiv(G[d], cand[d]) for d in range(r)]
+            fl, rows = self.flags_for(prog, cand, tiles)
+            if rows * cand[r - 1] > d_["cap_elems"]:
+                continue
+            stage, hoist, _, _ = self.layout(prog, fl)
+            if 2 * stage + hoist > d_["smem_budget"]:
+                continue
+            ntiles = 1
+            for x in tiles:
+                ntiles *= x
+            waves = cdiv(ntiles, d_["num_cores"])
+            tb = 0
+            for ten in prog["tensors"]:
+                cover = 1
+                for d in range(r):
+                    if ten["vs"][d] != 0:
+                        cover *= cand[d]
+                tb += ESZ[ten["dtype"]] * cover
+            cost = waves * (d_["c0_bytes"] + tb)
+            if best is None or cost < best[0]:
+                best = (cost, cand)
+        if best is None:
+            raise EncodeError("capacity")
+        t = best[1]
+        tiles = [cdiv(G[d], t[d]) for d in range(r)]
+        fl, rows = self.flags_for(prog, t, tiles)
+        stage, hoist, soffs, hoff = self.layout(prog, fl)
+        for body, so in zip(prog["bodies"], soffs):
+            seen = set()
+            for ins in body:
+                if ins["op"] != I_LD:
+                    continue
+                ti = ins["b"]
+                f = fl[ti]
+                flags = ((L_DMA if f["dma"] else 0) | (L_HOIST if f["hoist"] else 0) |
+                         (L_COLV if f["colv"] else 0) | (L_ROWV if f["rowv"] else 0))
+                if f["dma"]:
+                    if ti not in seen:
+                        flags |= L_FIRST
+                        seen.add(ti)
+                    ins["aux0"] = hoff[ti] if f["hoist"] else so[ti]
+                ins["flags"] = flags
+        ntiles = 1
+        for x in tiles:
+            ntiles *= x
+        prog.update(t=t, block_dim=ntiles, stage_bytes=stage, hoist_bytes=hoist, K=0)
+
+    def plan_cube(self, prog):
+        d_ = self.desc
+        M, N = prog["G"]
+        mm_body = prog["bodies"][0]
+        mma = mm_body[0]
+        ta = prog["tensors"][mma["a"]]
+        tw = prog["tensors"][mma["b"]]
+        K = self.values[ta["vid"]].shape[1]
+        out_esz = 4
+        for ins in mm_body:
+            if ins["op"] == I_ST:
+                out_esz = min(out_esz, ESZ[prog["tensors"][ins["a"]]["dtype"]])
+        best = None
+        k = 1
+        while True:
+            c = cdiv(N, k)
+            tn = round_up(c, 16)
+            if tn <= 256:
+                tiles = cdiv(M, 128) * cdiv(N, tn)
+                waves = cdiv(tiles, d_["num_cores"])
+                flops = 2 * 128 * tn * K
+                tb = (128 + tn) * K * 2 + 128 * tn * out_esz
+                cost = waves * max(cdiv(flops, d_["flops_per_byte"]), tb)
+                if best is None or cost < best[0]:
+                    best = (cost, tn, tiles)
+            if tn <= 16:
+                break
+            k *= 2
+        _, tn, tiles = best
+        # every epilogue load is direct in the cube VM
+        for ins in mm_body:
+            if ins["op"] == I_LD:
+                ten = prog["tensors"][ins["b"]]
+                ins["flags"] = L_ROWV if ten["vs"][1] == 0 else 0
+        stage = (128 + tn) * 64 * 2
+        prog.update(t=[128, tn], block_dim=tiles, stage_bytes=stage, hoist_bytes=0, K=K)
+
+    # -- bytes
+    def encode(self, li):
+        launch = self.launches[li]
+        progs = [self.build_program(gi) for gi in launch]
+        d_ = self.desc
+        binds = []
+        for p in progs:
+            for t in p["tensors"]:
+                if t["vid"] not in binds:
+                    binds.append(t["vid"])
+        if len(binds) > MAX_BIND:
+            raise EncodeError("too many bindings")
+        kernel_type = KT_CUBE if progs[0]["kind"] == CUBE else KT_VEC
+        coop = any(p["kind"] == SEC for p in progs)
+        # instruction streams
+        streams = []
+        for p in progs:
+            words = []
+            if p["kind"] == SEC:
+                bodies = [self.with_syncs(b) for b in p["bodies"]]
+                A = bodies[0]
+                words.append(dict(op=I_TILES, imm=len(A)))
+                words += A
+                words.append(dict(op=I_GSUM))
+                if p["sst"] is not None:
+                    words.append(dict(op=I_SST, a=p["sst"]))
+                if len(bodies) == 1:
+                    pass
+                elif len(bodies) == 3:
+                    T, E = bodies[1], bodies[2]
+                    words.append(dict(op=I_JLE0, imm=len(T) + 2))
+                    words.append(dict(op=I_TILES, imm=len(T)))
+                    words += T
+                    words.append(dict(op=I_JMP, imm=len(E) + 1))
+                    words.append(dict(op=I_TILES, imm=len(E)))
+                    words += E
+                else:
+                    C = bodies[1]
+                    words.append(dict(op=I_TILES, imm=len(C)))
+                    words += C
+            else:
+                b = self.with_syncs(p["bodies"][0])
+                words.append(dict(op=I_TILES, imm=len(b)))
+                words += b
+            words.append(dict(op=I_END))
+            if len(words) > MAX_INSTR:
+                raise EncodeError("too many instructions")
+            streams.append(words)
+        stage = max(p["stage_bytes"] for p in progs)
+        hoist_total = sum(p["hoist_bytes"] for p in progs)
+        if kernel_type == KT_CUBE:
+            n_stages = min(d_["max_stages"], d_["smem_budget"] // stage)
+        else:
+            n_stages = min(d_["max_stages"], (d_["smem_budget"] - hoist_total) // stage) if stage else 0
+        # offsets
+        off = 48 + 64 * len(progs)
+        tens_offs = []
+        for p in progs:
+            tens_offs.append(off)
+            off += round_up(40 * len(p["tensors"]), 16)
+        body_offs = []
+        for s in streams:
+            body_offs.append(off)
+            off += 16 * len(s)
+        total = off
+        if total > MAX_IMAGE:
+            raise EncodeError("image too large")
+        block_dim = sum(p["block_dim"] for p in progs)
+        grid = d_["num_cores"]
+        out = bytearray()
+        out += struct.pack("<IHBBIHHIIIBBHIIII", MAGIC, 1, kernel_type, 1 if coop else 0, total,
+                           len(progs), len(binds), grid, block_dim, cdiv(block_dim, grid),
+                           progs[0]["a"] // 32, n_stages, d_["n_slots"], stage, hoist_total, 0, 0)
+        base = 0
+        hbase = 0
+        for p, to, bo, s in zip(progs, tens_offs, body_offs, streams):
+            n4 = list(p["G"]) + [1] * (4 - p["rank"])
+            t4 = list(p["t"]) + [1] * (4 - p["rank"])
+            out += struct.pack("<IIBBBBIII", p["block_dim"], base, p["rank"], len(p["tensors"]),
+                               p["kind"], 0, bo, len(s), to)
+            out += struct.pack("<4I", *n4) + struct.pack("<4I", *t4)
+            out += struct.pack("<II", p["K"], hbase)
+            base += p["block_dim"]
+            hbase += p["hoist_bytes"]
+        for p in progs:
+            tb = bytearray()
+            for t in p["tensors"]:
+                vs4 = list(t["vs"]) + [0] * (4 - p["rank"])
+                tb += struct.pack("<BBHI4q", t["dtype"], binds.index(t["vid"]), 0, 0, *vs4)
+            tb += b"\0" * (round_up(len(tb), 16) - len(tb))
+            out += tb
+        for s in streams:
+            for w in s:
+                out += struct.pack("<BBBBIII", w["op"], w.get("a", 0), w.get("b", 0), w.get("flags", 0),
+                                   w.get("imm", 0) & 0xFFFFFFFF, w.get("aux0", 0), 0)
+        assert len(out) == total
+        return bytes(out), binds
+
+    @staticmethod
+    def with_syncs(body):
+        idx = [i for i, w in enumerate(body) if w["op"] == I_LD and (w["flags"] & L_DMA) and not (w["flags"] & L_HOIST)]
+        if not idx:
+            return list(body)
+        first, last = idx[0], idx[-1]
+        out = []
+        for i, w in enumerate(body):
+            if i == first:
+                out.append(dict(op=I_WAIT))
+            out.append(w)
+            if i == last:
+                out.append(dict(op=I_REL))
+        return out
+
+
+# --------------------------------------------------------------- helpers --
+DT = {"f32": F32, "bf16": BF16, "u8": U8}
+
+
+def replay(ops, inputs, outputs, desc=None, shapes=None):
+    """Feed a workload op list through the reference fuser; returns (ctx, ids).
+
+    ops     : (op, input_names, out_name, out_dtype, attrs) tuples
+    inputs  : name -> (dtype string, shape, strides or None)
+    outputs : names to mark as outputs
+    Stops at the end of the list; the caller flushes.
+    """
+    ctx = RefCtx(desc)
+    ids = {}
+    for name, (dt, shape, strides) in inputs.items():
+        ids[name] = ctx.input(DT[dt], list(shape), strides)
+    launches = []
+    ctx.plans = {}
+    for op, ins, out, dt, attrs in ops:
+        if op == "opaque":
+            ctx.graph_add("opaque", [], [], DT[dt])
+            n = ctx.flush()
+            launches += [ctx.encode(i) for i in range(n)]
+            continue
+        shp = ctx.infer_shape(OPS[op], [ids[i] for i in ins], shapes.get(out) if shapes else None)
+        ids[out] = ctx.graph_add(op, [ids[i] for i in ins], shp, DT[dt], attrs)
+        if out in outputs:
+            ctx.mark_output(ids[out])
+    n = ctx.flush()
+    launches += [ctx.encode(i) for i in range(n)]
+    return ctx, ids, launches

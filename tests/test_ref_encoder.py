@@ -1,0 +1,209 @@
+"""The reference encoder against the pages and against the op-graph evaluator (CPU).
+
+* structure the pages fix: the vector-vector fusion example c = a + b; c = sqrt(c)
+  becomes one program Load, Load, Add, Sqrt, Store (review page section 5.1); the
+  header's block_dim is the tile count and body_tile the per-core count (sections
+  4.3-4.4); tiles are aligned to the instruction width and cover the iteration space;
+* pattern counts of the streaming fuser (elemwise-elemwise, reduce-forward,
+  matmul+elemwise; MindSpore summary section 3.3; spatial/temporal stacking, review
+  page section 5.1);
+* meaning: every encoded image, run by the numpy bytecode interpreter, reproduces the
+  op-graph evaluator within the path's tolerances.
+"""
+import struct
+
+import numpy as np
+import pytest
+
+from oracle import ref_encoder as R
+from oracle.bytecode_interp import parse, run_image
+from oracle.bf16 import bf16_bits_to_f64
+from oracle.evaluator import evaluate
+from bytecode_vm_jit_gb300 import workloads as W
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+DT = {"f32": 1, "bf16": 2, "u8": 3}
+
+
+def f64(arr, dt):
+    return bf16_bits_to_f64(arr) if dt == "bf16" else np.asarray(arr, np.float64)
+
+
+def run_through_vm_model(ops, inputs, outputs, desc=None, strides=None):
+    """Encode with the reference encoder, execute with the numpy interpreter."""
+    strides = strides or {}
+    spec = {k: (dt, np.shape(a), strides.get(k)) for k, (a, dt) in inputs.items()}
+    ctx, ids, launches = R.replay(ops, spec, outputs, desc)
+    store = {}
+    for name, (a, dt) in inputs.items():
+        store[ids[name]] = f64(a, dt).reshape(-1).copy() if name not in strides else f64(a, dt).T.reshape(-1).copy()
+    for img, binds in launches:
+        bufs = []
+        for v in binds:
+            val = ctx.values[v]
+            if v not in store:
+                store[v] = np.zeros(int(np.prod(val.shape)))
+            bufs.append((store[v], val.dtype))
+        run_image(img, bufs)
+    return {name: store[ids[name]].reshape(ctx.values[ids[name]].shape) for name in outputs}, launches
+
+
+def body_ops(img, p=0):
+    _, progs = parse(img)
+    return [w["op"] for w in progs[p]["body"]]
+
+
+def test_vector_vector_example_is_load_load_add_sqrt_store():
+    inp = W.sqrt_add_inputs((64, 300))
+    spec = {k: (dt, np.shape(a), None) for k, (a, dt) in inp.items()}
+    _, _, launches = R.replay(W.SQRT_ADD_OPS, spec, W.SQRT_ADD_OUT)
+    assert len(launches) == 1
+    ops = [o for o in body_ops(launches[0][0]) if o not in (R.I_WAIT, R.I_REL, R.I_TILES, R.I_END)]
+    assert ops == [R.I_LD, R.I_LD, 0x20, 0x10, R.I_ST]
+
+
+@pytest.mark.parametrize("shape", [(4096, 1024), (1, 1), (7, 129), (3, 5, 130), (2, 3, 4, 257), (1000,)])
+def test_header_counts_and_tile_alignment(shape):
+    spec = {"a": ("f32", shape, None), "b": ("f32", shape, None)}
+    _, _, launches = R.replay(W.SQRT_ADD_OPS, spec, W.SQRT_ADD_OUT)
+    hdr, progs = parse(launches[0][0])
+    p = progs[0]
+    r = p["rank"]
+    tiles = 1
+    for d in range(r):
+        tiles *= -(-p["n"][d] // p["t"][d])
+    assert hdr["block_dim"] == tiles == p["block_dim"]
+    assert hdr["body_tile"] == -(-tiles // hdr["grid"])
+    assert p["t"][r - 1] % (32 * hdr["ve"]) == 0
+    rows = 1
+    for d in range(r - 1):
+        assert 1 <= p["t"][d] <= p["n"][d]
+        rows *= p["t"][d]
+    assert rows * p["t"][r - 1] <= R.DEFAULT_DESC["cap_elems"]
+    assert p["n"][:r] == list(shape)
+
+
+def _counts(ops, inputs, outs, strides=None):
+    spec = {k: (dt, s, (strides or {}).get(k)) for k, (dt, s) in inputs.items()}
+    ctx, _, launches = R.replay(ops, spec, outs)
+    progs = [parse(img)[1] for img, _ in launches]
+    return launches, progs
+
+
+def test_fusion_counts_per_workload():
+    l, p = _counts(W.LAYERNORM_OPS, {"x": ("f32", (77, 4096)), "gamma": ("f32", (4096,)),
+                                     "beta": ("f32", (4096,))}, W.LAYERNORM_OUT)
+    assert len(l) == 1 and len(p[0]) == 1
+    l, p = _counts(W.IF_ELSE_ADD_OPS, {"x": ("bf16", (64, 8192)), "z": ("bf16", (64, 8192))}, W.IF_ELSE_ADD_OUT)
+    assert len(l) == 1 and p[0][0]["kind"] == R.SEC
+    assert R.I_JLE0 in body_ops(l[0][0]) and R.I_GSUM in body_ops(l[0][0])
+    l, p = _counts(W.MATMUL_ABS_OPS, {"A": ("bf16", (33, 4096)), "W": ("bf16", (4096, 4096)),
+                                      "bias": ("bf16", (4096,))}, W.MATMUL_ABS_OUT,
+                   strides={"W": [1, 4096]})
+    assert len(l) == 1 and parse(l[0][0])[0]["kernel_type"] == R.KT_CUBE
+    l, p = _counts(W.QWEN_STEP_OPS, {"x": ("bf16", (130, 5120)), "r": ("bf16", (130, 5120)),
+                                     "w": ("bf16", (5120,)), "g": ("bf16", (130, 17408)),
+                                     "u": ("bf16", (130, 17408))}, W.QWEN_STEP_OUT)
+    # two programs (RMSNorm group, SwiGLU group), stacked in one launch
+    assert len(l) == 1 and len(p[0]) == 2
+    # the add+relu+sum graph of the Triton-JIT page (section 3.2) fuses into one program
+    ops = [("adds", ["x"], "a", "f32", (1.0, 0)), ("maxs", ["a"], "b", "f32", (0.0, 0)),
+           ("reduce_sum", ["b"], "c", "f32", ())]
+    l, p = _counts(ops, {"x": ("f32", (33, 1000))}, ["c"])
+    assert len(l) == 1 and len(p[0]) == 1
+
+
+def test_dependent_groups_are_not_stacked():
+    ops = [("exp", ["x"], "e", "f32", ()),
+           ("reduce_sum", ["e"], "s", "f32", ()),
+           ("mul", ["y", "s"], "o", "f32", ())]
+    # y has a different inner extent, so "mul" starts a new group that reads s
+    l, p = _counts(ops, {"x": ("f32", (8, 256)), "y": ("f32", (8, 512))}, ["o"])
+    assert len(l) == 2
+    # a row-shaped consumer joins the reduce's group instead
+    l, p = _counts(ops, {"x": ("f32", (8, 256)), "y": ("f32", (8, 1))}, ["o"])
+    assert len(l) == 1 and len(p[0]) == 1
+
+
+def test_ragged_and_strided_views_are_direct_loads():
+    ops = [("add", ["a", "b"], "c", "f32", ())]
+    l, p = _counts(ops, {"a": ("f32", (5, 7)), "b": ("f32", (5, 7))}, ["c"])
+    lds = [w for w in p[0][0]["body"] if w["op"] == R.I_LD]
+    assert all(not (w["flags"] & R.L_DMA) for w in lds)       # 7*4 bytes is not a 16-B multiple
+    l, p = _counts(ops, {"a": ("f32", (64, 64)), "b": ("f32", (64, 64))}, ["c"], strides={"a": [1, 64]})
+    lds = [w for w in p[0][0]["body"] if w["op"] == R.I_LD]
+    assert [bool(w["flags"] & R.L_DMA) for w in lds] == [False, True]
+
+
+# --------------------------------------------------------- semantics -------
+def _cmp(got, ref, rel, floor=1.0):
+    scale = np.maximum(floor, np.abs(ref))
+    err = np.abs(got - ref) / scale
+    both_nan = np.isnan(got) & np.isnan(ref)
+    assert np.all((err <= rel) | both_nan), float(np.nanmax(err))
+
+
+def test_interp_sqrt_add():
+    inp = W.sqrt_add_inputs((37, 260))
+    got, _ = run_through_vm_model(W.SQRT_ADD_OPS, inp, W.SQRT_ADD_OUT)
+    ref = evaluate(W.SQRT_ADD_OPS, inp)
+    _cmp(got["y"], ref["y"], 1e-6)
+
+
+@pytest.mark.parametrize("rows", [1, 3, 40])
+def test_interp_layernorm(rows):
+    inp = W.layernorm_inputs(rows, rows)
+    got, _ = run_through_vm_model(W.LAYERNORM_OPS, inp, W.LAYERNORM_OUT)
+    ref = evaluate(W.LAYERNORM_OPS, inp)
+    _cmp(got["y"], ref["y"], 1e-5)
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3])
+def test_interp_if_else(i):
+    inp = W.if_else_inputs(i, 70, d=1024)
+    got, _ = run_through_vm_model(W.IF_ELSE_ADD_OPS, inp, W.IF_ELSE_ADD_OUT)
+    ref = evaluate(W.IF_ELSE_ADD_OPS, inp)
+    assert np.array_equal(got["y"], ref["y"])
+
+
+def test_interp_matmul_abs():
+    rng = np.random.default_rng(0)
+    k, n, m = 192, 160, 70
+    wt = W.f32_to_bf16_bits(rng.standard_normal((n, k)).astype(np.float32) * 0.02)
+    bias = W.f32_to_bf16_bits(rng.standard_normal(n).astype(np.float32) * 0.1)
+    a = W.f32_to_bf16_bits(rng.standard_normal((m, k)).astype(np.float32) * 0.02)
+    inp = {"A": (a, "bf16"), "W": (wt.T, "bf16"), "bias": (bias, "bf16")}
+    got, _ = run_through_vm_model(W.MATMUL_ABS_OPS, inp, W.MATMUL_ABS_OUT, strides={"W": [1, k]})
+    ref = evaluate(W.MATMUL_ABS_OPS, {"A": (a, "bf16"), "W": (np.ascontiguousarray(wt.T), "bf16"),
+                                      "bias": (bias, "bf16")})
+    rms = np.sqrt(np.mean(ref["y"] ** 2))
+    assert np.all(np.abs(got["y"] - ref["y"]) <= 2e-2 * np.maximum(np.abs(ref["y"]), rms))
+
+
+def test_interp_qwen_step():
+    inp = W.qwen_inputs(0, 5, hidden=512, inter=768)
+    got, _ = run_through_vm_model(W.QWEN_STEP_OPS, inp, W.QWEN_STEP_OUT)
+    ref = evaluate(W.QWEN_STEP_OPS, inp)
+    for k in W.QWEN_STEP_OUT:
+        rms = np.sqrt(np.mean(ref[k] ** 2))
+        assert np.all(np.abs(got[k] - ref[k]) <= 2e-2 * np.maximum(np.abs(ref[k]), rms)), k
+
+
+def test_interp_mixed_ops_and_row_values():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((9, 300)).astype(np.float32)
+    c = rng.standard_normal((9, 1)).astype(np.float32)
+    ops = [("reduce_max", ["x"], "m", "f32", ()),
+           ("sub", ["x", "m"], "d", "f32", ()),
+           ("exp", ["d"], "e", "f32", ()),
+           ("reduce_sum", ["e"], "s", "f32", ()),
+           ("div", ["e", "s"], "p", "f32", ()),          # softmax
+           ("mul", ["p", "c"], "q", "f32", ()),
+           ("subs", ["q"], "o", "f32", (1.0, 1)),        # 1 - q
+           ("abs", ["o"], "o2", "f32", ()),
+           ("log", ["o2"], "o3", "f32", ())]
+    inp = {"x": (x, "f32"), "c": (c, "f32")}
+    got, _ = run_through_vm_model(ops, inp, ["o3", "s"])
+    ref = evaluate(ops, inp)
+    _cmp(got["o3"], ref["o3"], 1e-5)
+    _cmp(got["s"], ref["s"], 1e-5)
