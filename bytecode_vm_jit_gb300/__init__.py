@@ -1,0 +1,326 @@
+"""Python binding of the DVM C ABI (`libdvm.so`, declared in include/dvm.h).
+
+Argument marshalling only: every step of the hot path (streaming fusion, tiling,
+encoding, the interpreter kernels) runs inside the library.  The functions below
+keep the C names; `Ctx` and `run_ops` add the bookkeeping a caller needs to feed an
+op stream and bind torch tensors (PyTorch provides device memory and streams).
+
+The library is loaded on first use and must have been built for sm_103a
+(`bytecode_vm_jit_gb300.build.build()`); there is no fallback if it is missing.
+"""
+import ctypes
+import os
+
+from . import build as _build
+
+DTYPES = {"f32": 1, "bf16": 2, "u8": 3}
+OPS = {
+    "copy": 1, "sqrt": 2, "abs": 3, "log": 4, "exp": 5, "round": 6, "floor": 7,
+    "isfinite": 8, "neg": 9, "rsqrt": 10, "recip": 11, "silu": 12, "cast": 13,
+    "broadcast": 14, "add": 20, "sub": 21, "mul": 22, "div": 23, "max": 24, "min": 25,
+    "pow": 26, "adds": 30, "subs": 31, "muls": 32, "divs": 33, "maxs": 34, "mins": 35,
+    "pows": 36, "reduce_sum": 40, "reduce_max": 41, "reduce_mean": 42,
+    "reduce_sum_all": 43, "select_gt0": 50, "matmul": 60, "opaque": 70,
+}
+STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_OP", -3: "SHAPE", -4: "BUF_TOO_SMALL",
+          -5: "BYTECODE", -6: "CUDA", -7: "STATE", -8: "CAPACITY", -100: "TIMEOUT",
+          -101: "BAD_OPCODE", -102: "BOUNDS"}
+EXPORTS = ["dvm_create", "dvm_create_host", "dvm_destroy", "dvm_reset", "dvm_get_desc", "dvm_input",
+           "dvm_graph_add", "dvm_mark_output", "dvm_value_info", "dvm_flush", "dvm_encode",
+           "dvm_validate", "dvm_run", "dvm_poll_status", "dvm_last_error", "dvm_stats",
+           "dvm_stats_reset_last", "dvm_debug_set_barrier"]
+
+MAX_IMAGE = 8192
+MAX_BIND = 16
+
+
+class DvmError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s (%d): %s" % (STATUS.get(code, "?"), code, msg))
+        self.code = code
+
+
+class DeviceDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_cores", "cap_elems", "smem_budget", "max_stages",
+                                              "c0_bytes", "flops_per_byte", "n_slots")]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("ops_added", "groups_closed", "flushes", "launches_encoded",
+                                              "programs_encoded", "runs", "host_ns_total", "host_ns_last")]
+
+
+_lib = None
+
+
+def lib():
+    """Load libdvm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libdvm.so not found at %s; run bytecode_vm_jit_gb300.build.build()" % _build.LIB)
+    L = ctypes.CDLL(_build.LIB)
+    P, I32, I64, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    L.dvm_create.argtypes = [P(VP), ctypes.c_int]
+    L.dvm_create_host.argtypes = [P(VP), P(DeviceDesc)]
+    L.dvm_destroy.argtypes = [VP]
+    L.dvm_destroy.restype = None
+    L.dvm_reset.argtypes = [VP]
+    L.dvm_get_desc.argtypes = [VP, P(DeviceDesc)]
+    L.dvm_input.argtypes = [VP, ctypes.c_int, ctypes.c_int, P(I64), P(I64), P(I32)]
+    L.dvm_graph_add.argtypes = [VP, ctypes.c_int, P(I32), ctypes.c_int, P(I64), ctypes.c_int, ctypes.c_int,
+                                P(ctypes.c_float), ctypes.c_int, P(I32)]
+    L.dvm_mark_output.argtypes = [VP, I32]
+    L.dvm_value_info.argtypes = [VP, I32, P(I32), P(I32), P(I64)]
+    L.dvm_flush.argtypes = [VP, P(I32)]
+    L.dvm_encode.argtypes = [VP, I32, ctypes.c_char_p, ctypes.c_size_t, P(ctypes.c_size_t), P(I32), P(I32)]
+    L.dvm_validate.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+    L.dvm_run.argtypes = [VP, ctypes.c_char_p, ctypes.c_size_t, P(VP), ctypes.c_int, VP]
+    L.dvm_poll_status.argtypes = [VP, VP, P(I32)]
+    L.dvm_last_error.argtypes = [VP]
+    L.dvm_last_error.restype = ctypes.c_char_p
+    L.dvm_stats.argtypes = [VP, P(Stats)]
+    L.dvm_stats_reset_last.argtypes = [VP]
+    L.dvm_debug_set_barrier.argtypes = [VP, ctypes.c_int, ctypes.c_int]
+    for n in EXPORTS:
+        f = getattr(L, n)
+        if n not in ("dvm_destroy", "dvm_last_error"):
+            f.restype = ctypes.c_int32
+    _lib = L
+    return L
+
+
+def _check(ctx, rc):
+    if rc != 0:
+        msg = lib().dvm_last_error(ctx).decode() if ctx else ""
+        raise DvmError(rc, msg)
+
+
+# ------------------------------------------------------------- C-named calls --
+def dvm_create(device=0):
+    h = ctypes.c_void_p()
+    rc = lib().dvm_create(ctypes.byref(h), int(device))
+    if rc != 0:
+        msg = lib().dvm_last_error(h).decode() if h else ""
+        if h:
+            lib().dvm_destroy(h)
+        raise DvmError(rc, msg)
+    return h
+
+
+def dvm_create_host(**desc):
+    d = DeviceDesc(num_cores=152, cap_elems=7680, smem_budget=196608, max_stages=8, c0_bytes=4096,
+                   flops_per_byte=280, n_slots=2)
+    for k, v in desc.items():
+        setattr(d, k, int(v))
+    h = ctypes.c_void_p()
+    _check(None, lib().dvm_create_host(ctypes.byref(h), ctypes.byref(d)))
+    return h
+
+
+def dvm_destroy(ctx):
+    lib().dvm_destroy(ctx)
+
+
+def dvm_reset(ctx):
+    _check(ctx, lib().dvm_reset(ctx))
+
+
+def dvm_input(ctx, dtype, shape, strides=None):
+    n = len(shape)
+    sh = (ctypes.c_int64 * n)(*shape)
+    st = (ctypes.c_int64 * n)(*strides) if strides is not None else None
+    out = ctypes.c_int32()
+    _check(ctx, lib().dvm_input(ctx, DTYPES[dtype], n, sh, st, ctypes.byref(out)))
+    return out.value
+
+
+def dvm_graph_add(ctx, op, inputs, dtype, attrs=(), shape=None):
+    code = OPS[op]
+    ins = (ctypes.c_int32 * max(1, len(inputs)))(*inputs)
+    if shape is None:
+        sh, rank = None, (0 if op == "opaque" else -1)
+    else:
+        sh, rank = (ctypes.c_int64 * max(1, len(shape)))(*shape), len(shape)
+    at = (ctypes.c_float * max(1, len(attrs)))(*attrs)
+    out = ctypes.c_int32()
+    _check(ctx, lib().dvm_graph_add(ctx, code, ins, len(inputs), sh, rank, DTYPES[dtype], at, len(attrs),
+                                     ctypes.byref(out)))
+    return out.value
+
+
+def dvm_mark_output(ctx, vid):
+    _check(ctx, lib().dvm_mark_output(ctx, int(vid)))
+
+
+def dvm_value_info(ctx, vid):
+    dt, rank = ctypes.c_int32(), ctypes.c_int32()
+    sh = (ctypes.c_int64 * 4)()
+    _check(ctx, lib().dvm_value_info(ctx, int(vid), ctypes.byref(dt), ctypes.byref(rank), sh))
+    return dt.value, tuple(sh[i] for i in range(rank.value))
+
+
+def dvm_flush(ctx):
+    n = ctypes.c_int32()
+    _check(ctx, lib().dvm_flush(ctx, ctypes.byref(n)))
+    return n.value
+
+
+_enc_buf = ctypes.create_string_buffer(MAX_IMAGE)
+_enc_ids = (ctypes.c_int32 * MAX_BIND)()
+
+
+def dvm_encode(ctx, launch):
+    ln = ctypes.c_size_t()
+    nt = ctypes.c_int32()
+    _check(ctx, lib().dvm_encode(ctx, int(launch), _enc_buf, MAX_IMAGE, ctypes.byref(ln), _enc_ids,
+                                 ctypes.byref(nt)))
+    return _enc_buf.raw[:ln.value], [_enc_ids[i] for i in range(nt.value)]
+
+
+def dvm_validate(image):
+    return lib().dvm_validate(image, len(image))
+
+
+def dvm_run(ctx, image, ptrs, stream=None):
+    n = len(ptrs)
+    arr = (ctypes.c_void_p * max(1, n))(*ptrs)
+    _check(ctx, lib().dvm_run(ctx, image, len(image), arr, n, stream))
+
+
+def dvm_poll_status(ctx, stream=None):
+    st = ctypes.c_int32()
+    _check(ctx, lib().dvm_poll_status(ctx, stream, ctypes.byref(st)))
+    return st.value
+
+
+def dvm_last_error(ctx):
+    return lib().dvm_last_error(ctx).decode()
+
+
+def dvm_stats(ctx):
+    s = Stats()
+    _check(ctx, lib().dvm_stats(ctx, ctypes.byref(s)))
+    return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+
+def dvm_stats_reset_last(ctx):
+    _check(ctx, lib().dvm_stats_reset_last(ctx))
+
+
+def dvm_debug_set_barrier(ctx, skip_one_arrival, timeout_ms=0):
+    _check(ctx, lib().dvm_debug_set_barrier(ctx, int(skip_one_arrival), int(timeout_ms)))
+
+
+# ---------------------------------------------------------------- helpers ----
+_TORCH_DT = None
+
+
+def _torch_dtype(code):
+    global _TORCH_DT
+    import torch
+    if _TORCH_DT is None:
+        _TORCH_DT = {1: torch.float32, 2: torch.bfloat16, 3: torch.uint8}
+    return _TORCH_DT[code]
+
+
+def _dt_name(t):
+    import torch
+    return {torch.float32: "f32", torch.bfloat16: "bf16", torch.uint8: "u8"}[t.dtype]
+
+
+class Ctx:
+    """A context plus the torch tensors bound to its values.
+
+    `feed(ops, inputs, outputs)` replays an op stream (tuples
+    (op, input_names, out_name, out_dtype, attrs)); an `opaque` op flushes and runs
+    the pending launches.  Tensors for values the launches write are allocated with
+    torch on the context's device.
+    """
+
+    def __init__(self, device=0, host_only=False, **desc):
+        self.host_only = host_only
+        self.h = dvm_create_host(**desc) if host_only else dvm_create(device)
+        self.device = device
+        self.tensors = {}     # value id -> torch tensor
+        self.ids = {}         # name -> value id
+        self.launch_log = []  # (image, binding ids) of every launch run
+
+    def close(self):
+        if self.h:
+            dvm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        dvm_reset(self.h)
+        self.tensors.clear()
+        self.ids.clear()
+
+    def bind_input(self, name, t):
+        vid = dvm_input(self.h, _dt_name(t), list(t.shape), list(t.stride()))
+        self.ids[name] = vid
+        self.tensors[vid] = t
+        return vid
+
+    def add(self, op, ins, out, dtype, attrs=()):
+        vid = dvm_graph_add(self.h, op, [self.ids[i] for i in ins], dtype, attrs)
+        if out:
+            self.ids[out] = vid
+        return vid
+
+    def run_pending(self, stream=None):
+        import torch
+        n = dvm_flush(self.h)
+        if stream is None and not self.host_only:
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        for i in range(n):
+            img, binds = dvm_encode(self.h, i)
+            ptrs = []
+            for vid in binds:
+                t = self.tensors.get(vid)
+                if t is None:
+                    dt, shape = dvm_value_info(self.h, vid)
+                    t = torch.empty(shape, dtype=_torch_dtype(dt), device="cuda:%d" % self.device)
+                    self.tensors[vid] = t
+                ptrs.append(t.data_ptr())
+            self.launch_log.append((img, binds))
+            if not self.host_only:
+                dvm_run(self.h, img, ptrs, stream)
+        return n
+
+    def feed(self, ops, inputs, outputs, stream=None):
+        for name, t in inputs.items():
+            self.bind_input(name, t)
+        for op, ins, out, dt, attrs in ops:
+            if op == "opaque":
+                dvm_graph_add(self.h, "opaque", [], dt)
+                self.run_pending(stream)
+                continue
+            self.add(op, ins, out, dt, attrs)
+            if out in outputs:
+                dvm_mark_output(self.h, self.ids[out])
+        self.run_pending(stream)
+        return {name: self.tensors[self.ids[name]] for name in outputs}
+
+    def poll(self, stream=None):
+        return dvm_poll_status(self.h, stream)
+
+
+def run_ops(ops, inputs, outputs, device=0, stream=None):
+    """Run an op stream on device tensors; returns the output tensors."""
+    ctx = Ctx(device)
+    try:
+        out = ctx.feed(ops, inputs, outputs, stream)
+        st = ctx.poll(stream)
+        if st != 0:
+            raise DvmError(st, "device status")
+        return out
+    finally:
+        ctx.close()

@@ -1,0 +1,75 @@
+"""Build the C-ABI library `libdvm.so` in-tree (bytecode_vm_jit_gb300/_build/).
+
+Host C++ (fuser, tiler, encoder, validator, C ABI) is compiled with g++; the CUDA
+interpreter kernels with nvcc for sm_103a only; all translation units compile in
+parallel and link into one shared library with the CUDA runtime linked statically.
+Nothing is compiled or loaded per shape at run time.
+
+Usage: python -m bytecode_vm_jit_gb300.build [--force]
+"""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(HERE, "csrc")
+OUT = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT, "libdvm.so")
+
+CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+CU_SOURCES = ["vm_vec4.cu", "vm_vec8.cu", "vm_vec16.cu", "vm_runtime.cu", "vm_cube.cu"]
+CPP_SOURCES = ["dvm_host.cpp"]
+HEADERS = ["dvm_format.h", "dvm_internal.h", "vm_common.cuh", "vm_vec.cuh"]
+
+
+def _newest(paths):
+    return max(os.path.getmtime(p) for p in paths)
+
+
+def _run(cmd):
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("build step failed: %s\n%s" % (" ".join(cmd), r.stdout))
+    return r.stdout
+
+
+def build(force=False, verbose=False):
+    """Compile every translation unit for sm_103a and link libdvm.so. Returns its path."""
+    os.makedirs(OUT, exist_ok=True)
+    headers = [os.path.join(SRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "dvm.h")]
+    hdr_time = _newest(headers)
+    jobs = []
+    objs = []
+    for src in CU_SOURCES + CPP_SOURCES:
+        path = os.path.join(SRC, src)
+        obj = os.path.join(OUT, src.rsplit(".", 1)[0] + ".o")
+        objs.append(obj)
+        if not force and os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(path), hdr_time):
+            continue
+        if src.endswith(".cu"):
+            cmd = [NVCC] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                                   "-Xptxas", "-v", "-c", path, "-o", obj]
+        else:
+            cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I" + os.path.join(CUDA_HOME, "include"),
+                   "-c", path, "-o", obj]
+        jobs.append(cmd)
+    logs = []
+    if jobs:
+        with ThreadPoolExecutor(max_workers=min(8, len(jobs))) as ex:
+            logs = list(ex.map(_run, jobs))
+    if force or jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < _newest(objs):
+        tmp = LIB + ".tmp"
+        _run([NVCC] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs)
+        os.replace(tmp, LIB)
+    if verbose:
+        for lg in logs:
+            sys.stdout.write(lg)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,117 @@
+// dvm_format.h — binary layout of a DVM launch image (host encoder <-> device VM).
+//
+// A launch image is the "bytecode program" of the DVM review page, section 4.3
+// (Fig 7): a code header (block_dim = number of tiles, body_tile = tiles per core,
+// kernel type) followed by the code body (one 16-byte word per tile instruction of
+// Table 1, section 4.1, plus the synchronisation words the encoder inserts).  Several
+// programs may share one launch (spatial/temporal stacking, section 5.1, Fig 9).
+// All fields are little-endian; the structs below are the in-memory view of the
+// bytes on both sides (x86-64/aarch64 hosts and the GPU are little-endian).
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define DVM_HD __host__ __device__
+#else
+#define DVM_HD
+#endif
+
+namespace dvm {
+
+constexpr uint32_t kMagic = 0x314D5644u;  // "DVM1"
+constexpr uint16_t kVersion = 1;
+constexpr int kMaxProgs = 4;
+constexpr int kMaxBind = 16;
+constexpr int kMaxTens = 16;
+constexpr int kMaxInstr = 96;
+constexpr int kMaxImage = 8192;
+constexpr int kNumSlots = 2;        // addressable register slots besides ACC
+constexpr int kVmWarps = 15;        // consumer warps of the VEC interpreter
+constexpr int kVmReg = 16;          // fp32 values per register slot per thread
+constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 7680 padded elements per tile
+constexpr int kMaxRank = 4;
+
+enum KernelType : uint8_t { KT_VEC = 1, KT_CUBE = 2 };
+enum ProgKind : uint8_t { PK_VEC = 0, PK_SEC = 1, PK_CUBE = 2 };
+enum HeaderFlags : uint8_t { HF_COOP = 1 };
+enum Dtype : uint8_t { DT_F32 = 1, DT_BF16 = 2, DT_U8 = 3 };
+
+// VM opcodes (one byte)
+enum Opcode : uint8_t {
+  OP_LD = 0x01, OP_ST = 0x02, OP_MOV = 0x03, OP_BCAST = 0x04, OP_WAIT = 0x05, OP_REL = 0x06,
+  OP_SQRT = 0x10, OP_ABS = 0x11, OP_LOG = 0x12, OP_EXP = 0x13, OP_ROUND = 0x14,
+  OP_FLOOR = 0x15, OP_ISFIN = 0x16, OP_NEG = 0x17, OP_RSQRT = 0x18, OP_RECIP = 0x19,
+  OP_SILU = 0x1A, OP_CASTBF = 0x1B,
+  OP_ADD = 0x20, OP_SUB = 0x21, OP_MUL = 0x22, OP_DIV = 0x23, OP_MAX = 0x24, OP_MIN = 0x25,
+  OP_POW = 0x26,
+  OP_RSUM = 0x30, OP_RMAX = 0x31, OP_ASUM = 0x32,
+  OP_TILES = 0x40, OP_GSUM = 0x41, OP_JLE0 = 0x42, OP_JMP = 0x43, OP_SST = 0x44, OP_END = 0x45,
+  OP_MMA = 0x50,
+};
+
+// LD / ST flags
+enum LoadFlags : uint8_t { LF_DMA = 1, LF_HOIST = 2, LF_COLV = 4, LF_ROWV = 8, LF_FIRST = 16 };
+// compute flags
+enum ComputeFlags : uint8_t { CF_AROW = 1, CF_XROW = 2, CF_REV = 4, CF_IMM = 8 };
+
+#pragma pack(push, 1)
+struct Header {            // 48 bytes
+  uint32_t magic;
+  uint16_t version;
+  uint8_t kernel_type;
+  uint8_t flags;
+  uint32_t total_len;
+  uint16_t n_progs;
+  uint16_t n_bind;
+  uint32_t grid;
+  uint32_t block_dim;
+  uint32_t body_tile;
+  uint8_t ve;
+  uint8_t n_stages;
+  uint16_t n_slots;
+  uint32_t stage_bytes;
+  uint32_t hoist_bytes;
+  uint32_t reserved0;
+  uint32_t reserved1;
+};
+struct ProgRec {           // 64 bytes
+  uint32_t block_dim;
+  uint32_t tile_base;
+  uint8_t rank;
+  uint8_t n_tens;
+  uint8_t kind;
+  uint8_t reserved;
+  uint32_t body_off;       // byte offset of the body in the image
+  uint32_t body_len;       // instructions
+  uint32_t tens_off;       // byte offset of the tensor table
+  uint32_t n[4];
+  uint32_t t[4];
+  uint32_t K;
+  uint32_t hoist_base;
+};
+struct TensRec {           // 40 bytes
+  uint8_t dtype;
+  uint8_t binding;
+  uint16_t reserved0;
+  uint32_t reserved1;
+  int64_t vs[4];
+};
+struct Instr {             // 16 bytes
+  uint8_t op;
+  uint8_t a;
+  uint8_t b;
+  uint8_t flags;
+  uint32_t imm;
+  uint32_t aux0;
+  uint32_t aux1;
+};
+#pragma pack(pop)
+
+static_assert(sizeof(Header) == 48, "header layout");
+static_assert(sizeof(ProgRec) == 64, "program record layout");
+static_assert(sizeof(TensRec) == 40, "tensor record layout");
+static_assert(sizeof(Instr) == 16, "instruction layout");
+
+DVM_HD inline int dtype_size(int dt) { return dt == DT_F32 ? 4 : dt == DT_BF16 ? 2 : 1; }
+
+}  // namespace dvm

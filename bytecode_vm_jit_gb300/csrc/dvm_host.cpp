@@ -1,0 +1,1575 @@
+// dvm_host.cpp — host half of the DVM hot path: op graph, streaming fuser, shape
+// tiler, bytecode encoder, validator and the C ABI.
+//
+// Method (DVM review page, arXiv 2603.24239):
+//   * dynamic-graph streaming fusion, section 5.2 (Fig 10): ops are appended to a
+//     buffer, fusion conditions (shape compatibility, dependencies) are checked at
+//     once, and the buffer is flushed when a new op cannot fuse or a sync point is
+//     reached (MindSpore DVM summary, section 3.2: unsupported op, fusion boundary or
+//     sync interface).  Patterns: elemwise-elemwise, reduce-forward, matmul+elemwise
+//     (MindSpore summary 3.3); stacking of independent programs (review 5.1, Fig 9).
+//   * shape tiling, section 4.2 (Fig 6): dominant shape S_d, start from the largest
+//     tile and shrink outer to inner, hardware_align_div rounds to the instruction
+//     width, resource constraints and a light cost model prune the plans.
+//   * bytecode format, section 4.3 (Fig 7): header (block_dim, body_tile, kernel
+//     type) + body (tile instructions of Table 1 and inserted syncs).
+// The exact byte layout, candidate order, cost model and lowering rules are this
+// library's own specification; the reference encoder on the test side implements the
+// same specification independently and the tests compare the bytes.
+//
+// Host hot loop budget: an op instance (graph_add x n, flush, encode) should take a
+// few microseconds; containers keep their capacity across instances.
+#include "dvm_format.h"
+#include "dvm_internal.h"
+#include "../../include/dvm.h"
+
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+using namespace dvm;
+
+namespace {
+
+// ----------------------------------------------------------------- helpers --
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+// tile extent for k parts of n, rounded up to the instruction width al
+inline int64_t hardware_align_div(int64_t n, int64_t k, int64_t al) { return round_up(cdiv(n, k), al); }
+
+inline uint32_t f32_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return u;
+}
+
+enum OpClass : int8_t { C_ELT, C_RRED, C_ARED, C_SEL, C_MM, C_OPQ, C_BAD };
+
+bool is_unary(int c) { return c >= 1 && c <= 14; }
+bool is_binary(int c) { return c >= 20 && c <= 26; }
+bool is_scalar(int c) { return c >= 30 && c <= 36; }
+bool is_rred(int c) { return c >= 40 && c <= 42; }
+
+OpClass op_class(int c) {
+  if (is_unary(c) || is_binary(c) || is_scalar(c)) return C_ELT;
+  if (is_rred(c)) return C_RRED;
+  if (c == 43) return C_ARED;
+  if (c == 50) return C_SEL;
+  if (c == 60) return C_MM;
+  if (c == 70) return C_OPQ;
+  return C_BAD;
+}
+
+uint8_t unary_vm(int c) {
+  switch (c) {
+    case 2: return OP_SQRT; case 3: return OP_ABS; case 4: return OP_LOG; case 5: return OP_EXP;
+    case 6: return OP_ROUND; case 7: return OP_FLOOR; case 8: return OP_ISFIN; case 9: return OP_NEG;
+    case 10: return OP_RSQRT; case 11: return OP_RECIP; case 12: return OP_SILU;
+    default: return 0;
+  }
+}
+uint8_t binary_vm(int c) { return (uint8_t)(OP_ADD + (c - 20)); }
+
+struct Shape {
+  int rank = 0;
+  int64_t d[4] = {1, 1, 1, 1};
+  bool operator==(const Shape& o) const {
+    if (rank != o.rank) return false;
+    for (int i = 0; i < rank; i++)
+      if (d[i] != o.d[i]) return false;
+    return true;
+  }
+  bool operator!=(const Shape& o) const { return !(*this == o); }
+  int64_t numel() const {
+    int64_t n = 1;
+    for (int i = 0; i < rank; i++) n *= d[i];
+    return n;
+  }
+};
+
+Shape rowshape(const Shape& g) {
+  Shape r = g;
+  r.d[r.rank - 1] = 1;
+  return r;
+}
+
+bool broadcast(const Shape& a, const Shape& b, Shape* out) {
+  int r = std::max(a.rank, b.rank);
+  Shape o;
+  o.rank = r;
+  for (int d = 0; d < r; d++) {
+    int ja = d - (r - a.rank), jb = d - (r - b.rank);
+    int64_t x = ja >= 0 ? a.d[ja] : 1, y = jb >= 0 ? b.d[jb] : 1;
+    if (x == y || y == 1) o.d[d] = x;
+    else if (x == 1) o.d[d] = y;
+    else return false;
+  }
+  *out = o;
+  return true;
+}
+
+struct Value {
+  int8_t dtype = 0;
+  Shape shape;
+  int64_t strides[4] = {0, 0, 0, 0};
+  int32_t producer = -1;  // op index
+  int32_t group = -1;
+  bool output = false;
+  bool used_outside = false;
+};
+
+struct Op {
+  int16_t code = 0;
+  OpClass cls = C_BAD;
+  int8_t n_in = 0;
+  int32_t in[3] = {-1, -1, -1};
+  int32_t out = -1;
+  int8_t dtype = 0;
+  float attrs[2] = {0.f, 0.f};
+  int8_t n_attrs = 0;
+  Shape shape;
+  bool reads(int32_t v) const {
+    for (int i = 0; i < n_in; i++)
+      if (in[i] == v) return true;
+    return false;
+  }
+  int count(int32_t v) const {
+    int c = 0;
+    for (int i = 0; i < n_in; i++) c += in[i] == v;
+    return c;
+  }
+};
+
+struct Group {
+  int8_t kind = PK_VEC;
+  Shape G;
+  std::vector<int32_t> ops;
+  int32_t ared = -1;
+  int32_t ared_pos = -1;
+  int32_t sel = -1;
+  bool has_rred = false;
+};
+
+// one body word before tensor indices are resolved
+struct Ins {
+  uint8_t op = 0, a = 0, b = 0, flags = 0;
+  uint32_t imm = 0, aux0 = 0;
+  int32_t tensor = -1;   // value id referenced by LD/ST
+  int32_t ta = -1, tb = -1;  // MMA operands (value ids)
+};
+
+struct Section {
+  std::vector<int32_t> ops;   // op indices
+  int32_t store_root = -1;    // value whose result is stored into store_as
+  int32_t store_as = -1;
+};
+
+struct Tensor {
+  int32_t vid;
+  int8_t dtype;
+  int64_t vs[4];
+};
+
+struct Program {
+  int32_t gi = -1;
+  int8_t kind = PK_VEC;
+  Shape G;
+  int a = 128;
+  std::vector<Tensor> tensors;
+  std::vector<std::vector<Ins>> bodies;
+  int32_t sst = -1;            // program-local tensor index or -1
+  int64_t t[4] = {1, 1, 1, 1};
+  int64_t block_dim = 0;
+  int64_t stage_bytes = 0;
+  int64_t hoist_bytes = 0;
+  int64_t K = 0;
+};
+
+struct EncodeFail {
+  int code;
+  const char* why;
+};
+
+}  // namespace
+
+// ===================================================================== ctx ==
+struct dvm_ctx {
+  dvm_device_desc desc{};
+  bool has_device = false;
+  DeviceState dev;
+  std::vector<Value> values;
+  std::vector<Op> ops;
+  std::vector<Group> groups;
+  int32_t open = -1;
+  std::vector<int32_t> pending;
+  std::vector<std::vector<int32_t>> launches;  // group indices per launch
+  std::vector<Program> plans;                  // indexed by group index
+  std::vector<uint8_t> plan_valid;
+  char err[256] = {0};
+  dvm_stats_t stats{};
+  // scratch reused by the lowering
+  std::vector<int32_t> rem;
+  std::vector<int8_t> slot_of;
+  std::vector<int8_t> kind_of;  // 0 unknown, 1 FULL, 2 ROW
+  std::vector<uint8_t> in_group;
+
+  int fail(int code, const char* fmt, const char* a = "") {
+    std::snprintf(err, sizeof err, fmt, a);
+    return code;
+  }
+};
+
+namespace {
+
+struct Timer {
+  dvm_ctx* c;
+  std::chrono::steady_clock::time_point t0;
+  explicit Timer(dvm_ctx* ctx) : c(ctx), t0(std::chrono::steady_clock::now()) {}
+  ~Timer() {
+    int64_t ns = std::chrono::duration_cast<std::chrono::nanoseconds>(
+                     std::chrono::steady_clock::now() - t0).count();
+    c->stats.host_ns_total += ns;
+    c->stats.host_ns_last += ns;
+  }
+};
+
+Shape iter_shape(const dvm_ctx* c, const Op& op) {
+  if (op.cls == C_RRED || op.cls == C_ARED) return c->values[op.in[0]].shape;
+  return op.shape;
+}
+
+// view strides of a value against iteration shape G (spec "Views")
+bool view_strides(const Value& v, const Shape& G, int64_t vs[4]) {
+  int r = G.rank, q = v.shape.rank;
+  if (q > r) return false;
+  for (int d = 0; d < 4; d++) vs[d] = 0;
+  for (int d = 0; d < r; d++) {
+    int j = d - (r - q);
+    if (j < 0 || v.shape.d[j] == 1) vs[d] = 0;
+    else if (v.shape.d[j] == G.d[d]) vs[d] = v.strides[j];
+    else return false;
+  }
+  return true;
+}
+
+void contiguous(Value& v) {
+  int64_t acc = 1;
+  for (int d = v.shape.rank - 1; d >= 0; d--) {
+    v.strides[d] = acc;
+    acc *= v.shape.d[d];
+  }
+}
+
+// ---------------------------------------------------------------- lowering --
+// Accumulator-machine lowering of one section (spec "Lowering").
+struct Lowering {
+  dvm_ctx* c;
+  const Shape& G;
+  const std::vector<int32_t>& ops;
+  const std::vector<uint8_t>* stored;  // indexed by value id (may be null)
+  int32_t store_root, store_as;
+  int n_slots;
+  std::vector<Ins>* body;
+  int32_t acc = -1;
+  // small maps keyed by value id (reset per lowering via the touched list)
+  std::vector<int32_t> touched;
+  bool free_[8] = {false, false, false, false, false, false, false, false};
+
+  Lowering(dvm_ctx* ctx, const Shape& g, const std::vector<int32_t>& o, const std::vector<uint8_t>* st,
+           int32_t root, int32_t as, int ns, std::vector<Ins>* out)
+      : c(ctx), G(g), ops(o), stored(st), store_root(root), store_as(as), n_slots(ns), body(out) {
+    for (int k = 1; k < 8; k++) free_[k] = k <= ns;
+    size_t nv = c->values.size();
+    if (c->rem.size() < nv) {
+      c->rem.resize(nv, 0);
+      c->slot_of.resize(nv, -1);
+      c->kind_of.resize(nv, 0);
+      c->in_group.resize(nv, 0);
+    }
+    for (int32_t oi : ops) {
+      const Op& op = c->ops[oi];
+      touch(op.out);
+      c->in_group[op.out] = 1;
+      if (op.cls == C_MM) continue;
+      for (int i = 0; i < op.n_in; i++) {
+        touch(op.in[i]);
+        c->rem[op.in[i]]++;
+      }
+    }
+  }
+  ~Lowering() {
+    for (int32_t v : touched) {
+      c->rem[v] = 0;
+      c->slot_of[v] = -1;
+      c->kind_of[v] = 0;
+      c->in_group[v] = 0;
+    }
+  }
+  void touch(int32_t v) {
+    if (c->kind_of[v] == 0 && c->slot_of[v] == -1 && c->rem[v] == 0 && !c->in_group[v]) {
+      touched.push_back(v);
+      c->kind_of[v] = -1;  // mark touched (value kind still unknown)
+    }
+  }
+  // 1 FULL, 2 ROW
+  int kind(int32_t v) {
+    int8_t k = c->kind_of[v];
+    if (k > 0) return k;
+    int64_t vs[4];
+    if (!view_strides(c->values[v], G, vs)) throw EncodeFail{DVM_E_SHAPE, "operand not broadcastable"};
+    return vs[G.rank - 1] == 0 ? 2 : 1;
+  }
+  bool external(int32_t v) { return !c->in_group[v]; }
+  int alloc() {
+    for (int k = 1; k <= n_slots; k++)
+      if (free_[k]) {
+        free_[k] = false;
+        return k;
+      }
+    throw EncodeFail{DVM_E_CAPACITY, "out of register slots"};
+  }
+  void emit(uint8_t op, uint8_t a = 0, uint8_t b = 0, uint8_t flags = 0, uint32_t imm = 0,
+            int32_t tensor = -1) {
+    Ins i;
+    i.op = op; i.a = a; i.b = b; i.flags = flags; i.imm = imm; i.tensor = tensor;
+    body->push_back(i);
+  }
+  void load(int32_t v, int dst) { emit(OP_LD, (uint8_t)dst, 0, 0, 0, v); }
+  void to_acc(int32_t v) {
+    if (acc == v) return;
+    if (c->slot_of[v] >= 0) {
+      emit(OP_MOV, 0, (uint8_t)c->slot_of[v], kind(v) == 2 ? 1 : 0);
+    } else if (external(v)) {
+      if (c->rem[v] == 1) {
+        load(v, 0);
+      } else {
+        int k = alloc();
+        load(v, k);
+        c->slot_of[v] = (int8_t)k;
+        emit(OP_MOV, 0, (uint8_t)k, kind(v) == 2 ? 1 : 0);
+      }
+    } else {
+      throw EncodeFail{DVM_E_CAPACITY, "lost value"};
+    }
+    acc = v;
+  }
+  int operand_slot(int32_t v) {
+    if (c->slot_of[v] >= 0) return c->slot_of[v];
+    int k = alloc();
+    if (external(v)) load(v, k);
+    else if (acc == v) emit(OP_MOV, (uint8_t)k, 0, kind(v) == 2 ? 1 : 0);
+    else throw EncodeFail{DVM_E_CAPACITY, "lost value"};
+    c->slot_of[v] = (int8_t)k;
+    return k;
+  }
+  bool is_stored(int32_t v) const { return stored && (size_t)v < stored->size() && (*stored)[v]; }
+
+  void run() {
+    size_t n = ops.size();
+    for (size_t i = 0; i < n; i++) {
+      const Op& op = c->ops[ops[i]];
+      int code = op.code;
+      int32_t r = op.out;
+      int rkind;
+      if (op.cls == C_MM) {
+        Ins w;
+        w.op = OP_MMA;
+        w.ta = op.in[0];
+        w.tb = op.in[1];
+        body->push_back(w);
+        rkind = 1;
+      } else if (is_binary(code)) {
+        int32_t p = op.in[0], q = op.in[1];
+        int x, rev;
+        if (acc == p && p != q) { x = operand_slot(q); rev = 0; }
+        else if (acc == q && p != q) { x = operand_slot(p); rev = 1; }
+        else if (p == q) { to_acc(p); x = operand_slot(p); rev = 0; }
+        else { to_acc(p); x = operand_slot(q); rev = 0; }
+        int kp = kind(p), kq = kind(q);
+        int ka = rev ? kq : kp, kx = rev ? kp : kq;
+        uint8_t fl = (uint8_t)((ka == 2 ? CF_AROW : 0) | (kx == 2 ? CF_XROW : 0) | (rev ? CF_REV : 0));
+        emit(binary_vm(code), (uint8_t)x, 0, fl);
+        rkind = (kp == 2 && kq == 2) ? 2 : 1;
+      } else {
+        int32_t p = op.in[0];
+        to_acc(p);
+        int kp = kind(p);
+        uint8_t af = kp == 2 ? CF_AROW : 0;
+        rkind = kp;
+        if (is_scalar(code)) {
+          bool left = op.n_attrs > 1 && op.attrs[1] != 0.f;
+          emit(binary_vm(code - 10), 0, 0, (uint8_t)(af | CF_IMM | (left ? CF_REV : 0)), f32_bits(op.attrs[0]));
+        } else if (unary_vm(code)) {
+          emit(unary_vm(code), 0, 0, af);
+        } else if (code == 1 || code == 13) {
+          // copy / cast: value unchanged (a bf16 cast rounds below)
+        } else if (code == 14) {
+          if (kp == 2 && op.shape.d[op.shape.rank - 1] != 1) {
+            emit(OP_BCAST);
+            rkind = 1;
+          }
+        } else if (is_rred(code)) {
+          if (kp == 1) {
+            emit(code == 41 ? OP_RMAX : OP_RSUM);
+            if (code == 42) {
+              const Value& pv = c->values[p];
+              emit(OP_DIV, 0, 0, CF_AROW | CF_IMM, f32_bits((float)pv.shape.d[pv.shape.rank - 1]));
+            }
+          }
+          rkind = 2;
+        } else if (code == 43) {
+          emit(OP_ASUM, 0, 0, af);
+          rkind = 2;
+        } else {
+          throw EncodeFail{DVM_E_UNSUPPORTED_OP, "op in body"};
+        }
+      }
+      acc = r;
+      c->kind_of[r] = (int8_t)rkind;
+      if (code != 43) {
+        if (op.dtype == DT_BF16) emit(OP_CASTBF, 0, 0, rkind == 2 ? CF_AROW : 0);
+        if (is_stored(r)) emit(OP_ST, 0, 0, rkind == 2 ? LF_ROWV : 0, 0, r);
+        if (r == store_root) emit(OP_ST, 0, 0, rkind == 2 ? LF_ROWV : 0, 0, store_as);
+      }
+      if (op.cls != C_MM) {
+        for (int j = 0; j < op.n_in; j++) {
+          int32_t v = op.in[j];
+          c->rem[v]--;
+        }
+        for (int j = 0; j < op.n_in; j++) {
+          int32_t v = op.in[j];
+          if (c->rem[v] == 0 && c->slot_of[v] >= 0) {
+            free_[(int)c->slot_of[v]] = true;
+            c->slot_of[v] = -1;
+          }
+        }
+      }
+      if (code == 43) continue;
+      int32_t rr = c->rem[r];
+      bool nxt = i + 1 < n && c->ops[ops[i + 1]].reads(r);
+      if (rr >= 2 || (rr == 1 && !nxt)) {
+        int k = alloc();
+        emit(OP_MOV, (uint8_t)k, 0, rkind == 2 ? 1 : 0);
+        c->slot_of[r] = (int8_t)k;
+      }
+    }
+    if ((int)body->size() > kMaxInstr - 2) throw EncodeFail{DVM_E_CAPACITY, "too many instructions"};
+  }
+};
+
+// ------------------------------------------------------------------ fuser --
+int min_esz_of_group(const dvm_ctx* c, const Group& g, int32_t extra) {
+  int m = 4;
+  auto visit = [&](int32_t oi) {
+    const Op& op = c->ops[oi];
+    m = std::min(m, dtype_size(op.dtype));
+    for (int i = 0; i < op.n_in; i++) m = std::min(m, dtype_size(c->values[op.in[i]].dtype));
+  };
+  for (int32_t oi : g.ops) visit(oi);
+  if (extra >= 0) visit(extra);
+  return m;
+}
+
+bool row_fits(const dvm_ctx* c, const Shape& G, int min_esz) {
+  int64_t a = 512 / min_esz;
+  return round_up(G.d[G.rank - 1], a) <= c->desc.cap_elems;
+}
+
+// section op lists of a (tentative) group; dry = no store targets
+void make_sections(const dvm_ctx* c, const std::vector<int32_t>& ops, bool dry, std::vector<Section>& out) {
+  out.clear();
+  int apos = -1;
+  for (size_t i = 0; i < ops.size(); i++)
+    if (c->ops[ops[i]].cls == C_ARED) { apos = (int)i; break; }
+  if (apos < 0) {
+    Section s;
+    s.ops = ops;
+    out.push_back(std::move(s));
+    return;
+  }
+  Section A;
+  A.ops.assign(ops.begin(), ops.begin() + apos + 1);
+  out.push_back(std::move(A));
+  std::vector<int32_t> post(ops.begin() + apos + 1, ops.end());
+  int32_t sel = -1;
+  for (int32_t oi : post)
+    if (c->ops[oi].cls == C_SEL) { sel = oi; break; }
+  if (sel < 0) {
+    if (!post.empty()) {
+      Section P;
+      P.ops = post;
+      out.push_back(std::move(P));
+    }
+    return;
+  }
+  std::vector<int32_t> body;
+  for (int32_t oi : post)
+    if (c->ops[oi].cls != C_SEL) body.push_back(oi);
+  const Op& so = c->ops[sel];
+  for (int br = 1; br <= 2; br++) {
+    int32_t root = so.in[br];
+    // transitive producers of root among body ops
+    std::vector<int32_t> need;
+    std::vector<int32_t> stack{root};
+    while (!stack.empty()) {
+      int32_t v = stack.back();
+      stack.pop_back();
+      int32_t prod = -1;
+      for (int32_t oi : body)
+        if (c->ops[oi].out == v) { prod = oi; break; }
+      if (prod < 0) continue;
+      if (std::find(need.begin(), need.end(), v) != need.end()) continue;
+      need.push_back(v);
+      const Op& po = c->ops[prod];
+      for (int i = 0; i < po.n_in; i++) stack.push_back(po.in[i]);
+    }
+    Section S;
+    for (int32_t oi : body)
+      if (std::find(need.begin(), need.end(), c->ops[oi].out) != need.end()) S.ops.push_back(oi);
+    if (!dry) {
+      S.store_root = root;
+      S.store_as = so.out;
+    }
+    out.push_back(std::move(S));
+  }
+}
+
+bool dry_run(dvm_ctx* c, const Group& g, int32_t extra) {
+  std::vector<int32_t> ops = g.ops;
+  ops.push_back(extra);
+  std::vector<Section> secs;
+  make_sections(c, ops, true, secs);
+  try {
+    for (const Section& s : secs) {
+      std::vector<Ins> body;
+      body.reserve(64);
+      Lowering L(c, g.G, s.ops, nullptr, -1, -1, c->desc.n_slots, &body);
+      L.run();
+    }
+  } catch (const EncodeFail&) {
+    return false;
+  }
+  return true;
+}
+
+bool accepts(dvm_ctx* c, int32_t gi, int32_t oi) {
+  Group& g = c->groups[gi];
+  const Op& op = c->ops[oi];
+  Shape isG = iter_shape(c, op);
+  if (op.cls == C_MM || op.cls == C_OPQ) return false;
+  if (g.kind == PK_CUBE) {
+    if (op.cls != C_ELT || isG != g.G) return false;
+    for (int i = 0; i < op.n_in; i++)
+      if (c->values[op.in[i]].shape.rank > 2) return false;
+  } else if (g.kind == PK_VEC) {
+    if (op.cls == C_ELT) {
+      if (isG != g.G && isG != rowshape(g.G)) return false;
+    } else if (op.cls == C_RRED) {
+      if (isG != g.G) return false;
+      if (!row_fits(c, g.G, min_esz_of_group(c, g, oi))) return false;
+    } else if (op.cls == C_ARED) {
+      if (isG != g.G || g.has_rred) return false;
+    } else {
+      return false;
+    }
+  } else {  // PK_SEC
+    if (g.sel >= 0) return false;
+    auto in_pre = [&](int32_t v) {
+      for (int j = 0; j <= g.ared_pos; j++)
+        if (c->ops[g.ops[j]].out == v) return true;
+      return false;
+    };
+    auto in_post = [&](int32_t v) {
+      for (size_t j = g.ared_pos + 1; j < g.ops.size(); j++)
+        if (c->ops[g.ops[j]].out == v) return true;
+      return false;
+    };
+    if (op.cls == C_ELT) {
+      if (isG != g.G) return false;
+      for (int i = 0; i < op.n_in; i++)
+        if (in_pre(op.in[i])) return false;
+    } else if (op.cls == C_SEL) {
+      if (op.in[0] != g.ared) return false;
+      for (int br = 1; br <= 2; br++) {
+        const Value& v = c->values[op.in[br]];
+        if (!in_post(op.in[br]) || v.shape != g.G || v.dtype != op.dtype) return false;
+      }
+    } else {
+      return false;
+    }
+  }
+  return dry_run(c, g, oi);
+}
+
+void append(dvm_ctx* c, int32_t gi, int32_t oi) {
+  Group& g = c->groups[gi];
+  const Op& op = c->ops[oi];
+  g.ops.push_back(oi);
+  c->values[op.out].group = gi;
+  if (op.cls == C_RRED) g.has_rred = true;
+  if (op.cls == C_ARED) {
+    g.ared = op.out;
+    g.ared_pos = (int32_t)g.ops.size() - 1;
+    g.kind = PK_SEC;
+  }
+  if (op.cls == C_SEL) g.sel = oi;
+  for (int i = 0; i < op.n_in; i++) {
+    Value& u = c->values[op.in[i]];
+    if (u.producer >= 0 && u.group != gi) u.used_outside = true;
+  }
+}
+
+void close_open(dvm_ctx* c) {
+  if (c->open >= 0) {
+    c->pending.push_back(c->open);
+    c->open = -1;
+    c->stats.groups_closed++;
+  }
+}
+
+int32_t start_group(dvm_ctx* c, int8_t kind, const Shape& G, int32_t oi) {
+  Group g;
+  g.kind = kind;
+  g.G = G;
+  g.ops.reserve(32);
+  c->groups.push_back(std::move(g));
+  c->open = (int32_t)c->groups.size() - 1;
+  append(c, c->open, oi);
+  return c->open;
+}
+
+// ----------------------------------------------------------- programs ------
+void stored_values(const dvm_ctx* c, int32_t gi, std::vector<uint8_t>& st) {
+  st.assign(c->values.size(), 0);
+  for (int32_t oi : c->groups[gi].ops) {
+    const Value& v = c->values[c->ops[oi].out];
+    if (v.output || v.used_outside) st[c->ops[oi].out] = 1;
+  }
+}
+
+int group_align(const dvm_ctx* c, int32_t gi) {
+  std::vector<uint8_t> st;
+  stored_values(c, gi, st);
+  int m = 4;
+  for (int32_t oi : c->groups[gi].ops) {
+    const Op& op = c->ops[oi];
+    for (int i = 0; i < op.n_in; i++)
+      if (c->values[op.in[i]].group != gi) m = std::min(m, dtype_size(c->values[op.in[i]].dtype));
+    if (st[op.out]) m = std::min(m, dtype_size(op.dtype));
+    if (op.cls == C_SEL) m = std::min(m, dtype_size(op.dtype));
+  }
+  return 512 / m;
+}
+
+struct LoadInfo {
+  bool dma, hoist, colv, rowv;
+  int64_t size;
+};
+
+void flags_for(const Program& p, const int64_t t[4], const int64_t tiles[4], LoadInfo* li, int64_t* rows_out) {
+  int r = p.G.rank;
+  int64_t rows = 1;
+  for (int d = 0; d < r - 1; d++) rows *= t[d];
+  for (size_t ti = 0; ti < p.tensors.size(); ti++) {
+    const Tensor& tn = p.tensors[ti];
+    int esz = dtype_size(tn.dtype);
+    bool rowv = tn.vs[r - 1] == 0;
+    bool dma = !rowv && tn.vs[r - 1] == 1 && (p.G.d[r - 1] * esz) % 16 == 0;
+    for (int d = 0; d < r - 1 && dma; d++)
+      if ((tn.vs[d] * esz) % 16 != 0) dma = false;
+    bool hoist = true;
+    for (int d = 0; d < r; d++)
+      if (tiles[d] > 1 && tn.vs[d] != 0) hoist = false;
+    bool colv = true;
+    for (int d = 0; d < r - 1; d++)
+      if (t[d] > 1 && tn.vs[d] != 0) colv = false;
+    li[ti].dma = dma;
+    li[ti].hoist = hoist;
+    li[ti].colv = colv;
+    li[ti].rowv = rowv;
+    li[ti].size = round_up((colv ? 1 : rows) * t[r - 1] * esz, 128);
+  }
+  *rows_out = rows;
+}
+
+// stage/hoist layout; returns stage max and hoist total; fills offsets when asked
+void layout(const Program& p, const LoadInfo* li, int64_t* stage_max, int64_t* hoist_total,
+            std::vector<std::vector<int64_t>>* soffs, std::vector<int64_t>* hoff) {
+  int nt = (int)p.tensors.size();
+  std::vector<int64_t> ho(nt, -1);
+  int64_t hoist = 0, smax = 0;
+  if (soffs) soffs->assign(p.bodies.size(), std::vector<int64_t>(nt, -1));
+  for (size_t bi = 0; bi < p.bodies.size(); bi++) {
+    int64_t off = 0;
+    std::vector<int64_t> so(nt, -1);
+    for (const Ins& w : p.bodies[bi]) {
+      if (w.op != OP_LD) continue;
+      int ti = w.b;
+      if (!li[ti].dma) continue;
+      if (li[ti].hoist) {
+        if (ho[ti] < 0) { ho[ti] = hoist; hoist += li[ti].size; }
+      } else if (so[ti] < 0) {
+        so[ti] = off;
+        off += li[ti].size;
+      }
+    }
+    smax = std::max(smax, off);
+    if (soffs) (*soffs)[bi] = so;
+  }
+  *stage_max = smax;
+  *hoist_total = hoist;
+  if (hoff) *hoff = ho;
+}
+
+void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
+  const dvm_device_desc& D = c->desc;
+  int r = p.G.rank;
+  const int64_t* n = p.G.d;
+  int64_t al[4] = {1, 1, 1, 1};
+  al[r - 1] = p.a;
+  int64_t t[4] = {1, 1, 1, 1};
+  for (int d = 0; d < r - 1; d++) t[d] = n[d];
+  t[r - 1] = hardware_align_div(n[r - 1], 1, p.a);
+  // candidate sequence: outer -> inner shrink
+  int64_t cands[256][4];
+  int nc = 0;
+  std::memcpy(cands[nc++], t, sizeof t);
+  for (int d = 0; d < r; d++) {
+    if (d == r - 1 && rowred) break;
+    for (int64_t k = 2;; k *= 2) {
+      int64_t cc = cdiv(n[d], k);
+      int64_t nt = round_up(cc, al[d]);
+      if (nt < t[d]) {
+        t[d] = nt;
+        if (nc < 256) std::memcpy(cands[nc++], t, sizeof t);
+      }
+      if (cc <= 1 || nt <= al[d]) break;
+    }
+  }
+  LoadInfo li[kMaxTens];
+  int best = -1;
+  int64_t best_cost = 0;
+  for (int ci = 0; ci < nc; ci++) {
+    const int64_t* cand = cands[ci];
+    int64_t tiles[4] = {1, 1, 1, 1};
+    for (int d = 0; d < r; d++) tiles[d] = cdiv(n[d], cand[d]);
+    int64_t rows;
+    flags_for(p, cand, tiles, li, &rows);
+    if (rows * cand[r - 1] > D.cap_elems) continue;
+    int64_t stage, hoist;
+    layout(p, li, &stage, &hoist, nullptr, nullptr);
+    if (2 * stage + hoist > D.smem_budget) continue;
+    int64_t ntiles = 1;
+    for (int d = 0; d < r; d++) ntiles *= tiles[d];
+    int64_t waves = cdiv(ntiles, D.num_cores);
+    int64_t tb = 0;
+    for (const Tensor& tn : p.tensors) {
+      int64_t cover = 1;
+      for (int d = 0; d < r; d++)
+        if (tn.vs[d] != 0) cover *= cand[d];
+      tb += dtype_size(tn.dtype) * cover;
+    }
+    int64_t cost = waves * (D.c0_bytes + tb);
+    if (best < 0 || cost < best_cost) {
+      best = ci;
+      best_cost = cost;
+    }
+  }
+  if (best < 0) throw EncodeFail{DVM_E_CAPACITY, "no feasible tiling"};
+  std::memcpy(p.t, cands[best], sizeof p.t);
+  int64_t tiles[4] = {1, 1, 1, 1};
+  for (int d = 0; d < r; d++) tiles[d] = cdiv(n[d], p.t[d]);
+  int64_t rows;
+  flags_for(p, p.t, tiles, li, &rows);
+  std::vector<std::vector<int64_t>> soffs;
+  std::vector<int64_t> hoff;
+  layout(p, li, &p.stage_bytes, &p.hoist_bytes, &soffs, &hoff);
+  for (size_t bi = 0; bi < p.bodies.size(); bi++) {
+    bool seen[kMaxTens] = {false};
+    for (Ins& w : p.bodies[bi]) {
+      if (w.op != OP_LD) continue;
+      int ti = w.b;
+      const LoadInfo& f = li[ti];
+      uint8_t fl = (uint8_t)((f.dma ? LF_DMA : 0) | (f.hoist ? LF_HOIST : 0) | (f.colv ? LF_COLV : 0) |
+                             (f.rowv ? LF_ROWV : 0));
+      if (f.dma) {
+        if (!seen[ti]) {
+          fl |= LF_FIRST;
+          seen[ti] = true;
+        }
+        w.aux0 = (uint32_t)(f.hoist ? hoff[ti] : soffs[bi][ti]);
+      }
+      w.flags = fl;
+    }
+  }
+  int64_t ntiles = 1;
+  for (int d = 0; d < r; d++) ntiles *= tiles[d];
+  p.block_dim = ntiles;
+  p.K = 0;
+}
+
+void plan_cube(const dvm_ctx* c, Program& p) {
+  const dvm_device_desc& D = c->desc;
+  int64_t M = p.G.d[0], N = p.G.d[1];
+  std::vector<Ins>& body = p.bodies[0];
+  const Ins& mma = body[0];
+  const Tensor& ta = p.tensors[mma.a];
+  int64_t K = c->values[ta.vid].shape.d[1];
+  int out_esz = 4;
+  for (const Ins& w : body)
+    if (w.op == OP_ST) out_esz = std::min(out_esz, dtype_size(p.tensors[w.a].dtype));
+  int64_t best_cost = -1, best_tn = 0, best_tiles = 0;
+  for (int64_t k = 1;; k *= 2) {
+    int64_t cc = cdiv(N, k);
+    int64_t tn = round_up(cc, 16);
+    if (tn <= 256) {
+      int64_t tiles = cdiv(M, 128) * cdiv(N, tn);
+      int64_t waves = cdiv(tiles, D.num_cores);
+      int64_t flops = 2 * 128 * tn * K;
+      int64_t tb = (128 + tn) * K * 2 + 128 * tn * out_esz;
+      int64_t cost = waves * std::max(cdiv(flops, D.flops_per_byte), tb);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_tn = tn;
+        best_tiles = tiles;
+      }
+    }
+    if (tn <= 16) break;
+  }
+  for (Ins& w : body)
+    if (w.op == OP_LD) w.flags = p.tensors[w.b].vs[1] == 0 ? LF_ROWV : 0;
+  p.t[0] = 128;
+  p.t[1] = best_tn;
+  p.t[2] = p.t[3] = 1;
+  p.block_dim = best_tiles;
+  p.stage_bytes = (128 + best_tn) * 64 * 2;
+  p.hoist_bytes = 0;
+  p.K = K;
+}
+
+void lower_group(dvm_ctx* c, int32_t gi, std::vector<std::vector<Ins>>& bodies) {
+  const Group& g = c->groups[gi];
+  std::vector<uint8_t> st;
+  stored_values(c, gi, st);
+  if (g.kind == PK_SEC && g.sel >= 0) {
+    for (size_t j = g.ared_pos + 1; j < g.ops.size(); j++) {
+      const Op& o = c->ops[g.ops[j]];
+      if (o.cls != C_SEL && st[o.out]) throw EncodeFail{DVM_E_UNSUPPORTED_OP, "branch value used outside the select"};
+    }
+  }
+  if (g.ared >= 0) st[g.ared] = 0;
+  std::vector<Section> secs;
+  make_sections(c, g.ops, false, secs);
+  bodies.clear();
+  for (const Section& s : secs) {
+    bodies.emplace_back();
+    bodies.back().reserve(64);
+    Lowering L(c, g.G, s.ops, &st, s.store_root, s.store_as, c->desc.n_slots, &bodies.back());
+    L.run();
+  }
+}
+
+Program& build_program(dvm_ctx* c, int32_t gi) {
+  if ((size_t)gi < c->plan_valid.size() && c->plan_valid[gi]) return c->plans[gi];
+  if (c->plans.size() < c->groups.size()) {
+    c->plans.resize(c->groups.size());
+    c->plan_valid.resize(c->groups.size(), 0);
+  }
+  Program& p = c->plans[gi];
+  p = Program();
+  const Group& g = c->groups[gi];
+  p.gi = gi;
+  p.kind = g.kind;
+  p.G = g.G;
+  lower_group(c, gi, p.bodies);
+  auto ref = [&](int32_t v) -> int {
+    for (size_t i = 0; i < p.tensors.size(); i++)
+      if (p.tensors[i].vid == v) return (int)i;
+    Tensor t;
+    t.vid = v;
+    t.dtype = c->values[v].dtype;
+    for (int d = 0; d < 4; d++) t.vs[d] = 0;
+    p.tensors.push_back(t);
+    return (int)p.tensors.size() - 1;
+  };
+  for (auto& body : p.bodies)
+    for (Ins& w : body) {
+      if (w.op == OP_MMA) {
+        w.a = (uint8_t)ref(w.ta);
+        w.b = (uint8_t)ref(w.tb);
+      } else if (w.tensor >= 0) {
+        int t = ref(w.tensor);
+        if (w.op == OP_LD) w.b = (uint8_t)t;
+        else w.a = (uint8_t)t;
+      }
+    }
+  if (g.kind == PK_SEC) {
+    std::vector<uint8_t> st;
+    stored_values(c, gi, st);
+    if (st[g.ared]) p.sst = ref(g.ared);
+  }
+  if ((int)p.tensors.size() > kMaxTens) throw EncodeFail{DVM_E_CAPACITY, "too many tensors"};
+  int min_esz = 4;
+  for (const Tensor& t : p.tensors) min_esz = std::min(min_esz, dtype_size(t.dtype));
+  p.a = 512 / min_esz;
+  int r = p.G.rank;
+  int32_t mm_a = -1, mm_w = -1;
+  if (g.kind == PK_CUBE) {
+    mm_a = c->ops[g.ops[0]].in[0];
+    mm_w = c->ops[g.ops[0]].in[1];
+  }
+  for (Tensor& t : p.tensors) {
+    const Value& v = c->values[t.vid];
+    if (t.vid == mm_a || t.vid == mm_w) {
+      for (int d = 0; d < 4; d++) t.vs[d] = d < v.shape.rank ? v.strides[d] : 0;
+    } else if (!view_strides(v, p.G, t.vs)) {
+      throw EncodeFail{DVM_E_SHAPE, "operand not broadcastable"};
+    }
+  }
+  (void)r;
+  if (g.kind == PK_CUBE) plan_cube(c, p);
+  else plan_vec(c, p, g.has_rred);
+  c->plan_valid[gi] = 1;
+  return p;
+}
+
+bool can_stack(dvm_ctx* c, const std::vector<int32_t>& launch, int32_t gi) {
+  const Group& g = c->groups[gi];
+  if (g.kind != PK_VEC) return false;
+  for (int32_t x : launch)
+    if (c->groups[x].kind != PK_VEC) return false;
+  if ((int)launch.size() >= kMaxProgs) return false;
+  if (group_align(c, gi) != group_align(c, launch[0])) return false;
+  for (int32_t oi : g.ops) {
+    const Op& op = c->ops[oi];
+    for (int i = 0; i < op.n_in; i++) {
+      const Value& u = c->values[op.in[i]];
+      if (u.group != gi && u.group >= 0 && std::find(launch.begin(), launch.end(), u.group) != launch.end())
+        return false;
+    }
+  }
+  std::vector<int32_t> all = launch;
+  all.push_back(gi);
+  std::vector<int32_t> binds;
+  int64_t stage = 0, hoist = 0;
+  for (int32_t x : all) {
+    Program& p = build_program(c, x);
+    for (const Tensor& t : p.tensors)
+      if (std::find(binds.begin(), binds.end(), t.vid) == binds.end()) binds.push_back(t.vid);
+    stage = std::max(stage, p.stage_bytes);
+    hoist += p.hoist_bytes;
+  }
+  if ((int)binds.size() > kMaxBind) return false;
+  return 2 * stage + hoist <= c->desc.smem_budget;
+}
+
+void with_syncs(const std::vector<Ins>& body, std::vector<Ins>& out) {
+  int first = -1, last = -1;
+  for (size_t i = 0; i < body.size(); i++) {
+    const Ins& w = body[i];
+    if (w.op == OP_LD && (w.flags & LF_DMA) && !(w.flags & LF_HOIST)) {
+      if (first < 0) first = (int)i;
+      last = (int)i;
+    }
+  }
+  out.clear();
+  for (size_t i = 0; i < body.size(); i++) {
+    if ((int)i == first) { Ins w; w.op = OP_WAIT; out.push_back(w); }
+    out.push_back(body[i]);
+    if ((int)i == last) { Ins w; w.op = OP_REL; out.push_back(w); }
+  }
+}
+
+Ins ctl(uint8_t op, uint32_t imm = 0, uint8_t a = 0) {
+  Ins w;
+  w.op = op;
+  w.imm = imm;
+  w.a = a;
+  return w;
+}
+
+// writes the image; returns its length (or throws)
+size_t encode_launch(dvm_ctx* c, const std::vector<int32_t>& launch, std::vector<uint8_t>& img,
+                     std::vector<int32_t>& binds) {
+  std::vector<Program*> progs;
+  for (int32_t gi : launch) progs.push_back(&build_program(c, gi));
+  binds.clear();
+  for (Program* p : progs)
+    for (const Tensor& t : p->tensors)
+      if (std::find(binds.begin(), binds.end(), t.vid) == binds.end()) binds.push_back(t.vid);
+  if ((int)binds.size() > kMaxBind) throw EncodeFail{DVM_E_CAPACITY, "too many bindings"};
+  uint8_t kernel_type = progs[0]->kind == PK_CUBE ? KT_CUBE : KT_VEC;
+  bool coop = false;
+  std::vector<std::vector<Ins>> streams;
+  std::vector<Ins> tmp;
+  for (Program* p : progs) {
+    std::vector<Ins> words;
+    if (p->kind == PK_SEC) {
+      coop = true;
+      std::vector<std::vector<Ins>> b(p->bodies.size());
+      for (size_t i = 0; i < p->bodies.size(); i++) with_syncs(p->bodies[i], b[i]);
+      words.push_back(ctl(OP_TILES, (uint32_t)b[0].size()));
+      words.insert(words.end(), b[0].begin(), b[0].end());
+      words.push_back(ctl(OP_GSUM));
+      if (p->sst >= 0) words.push_back(ctl(OP_SST, 0, (uint8_t)p->sst));
+      if (b.size() == 3) {
+        words.push_back(ctl(OP_JLE0, (uint32_t)(b[1].size() + 2)));
+        words.push_back(ctl(OP_TILES, (uint32_t)b[1].size()));
+        words.insert(words.end(), b[1].begin(), b[1].end());
+        words.push_back(ctl(OP_JMP, (uint32_t)(b[2].size() + 1)));
+        words.push_back(ctl(OP_TILES, (uint32_t)b[2].size()));
+        words.insert(words.end(), b[2].begin(), b[2].end());
+      } else if (b.size() == 2) {
+        words.push_back(ctl(OP_TILES, (uint32_t)b[1].size()));
+        words.insert(words.end(), b[1].begin(), b[1].end());
+      }
+    } else {
+      with_syncs(p->bodies[0], tmp);
+      words.push_back(ctl(OP_TILES, (uint32_t)tmp.size()));
+      words.insert(words.end(), tmp.begin(), tmp.end());
+    }
+    words.push_back(ctl(OP_END));
+    if ((int)words.size() > kMaxInstr) throw EncodeFail{DVM_E_CAPACITY, "too many instructions"};
+    streams.push_back(std::move(words));
+  }
+  const dvm_device_desc& D = c->desc;
+  int64_t stage = 0, hoist_total = 0, block_dim = 0;
+  for (Program* p : progs) {
+    stage = std::max(stage, p->stage_bytes);
+    hoist_total += p->hoist_bytes;
+    block_dim += p->block_dim;
+  }
+  int64_t n_stages;
+  if (kernel_type == KT_CUBE) n_stages = std::min<int64_t>(D.max_stages, D.smem_budget / stage);
+  else n_stages = stage ? std::min<int64_t>(D.max_stages, (D.smem_budget - hoist_total) / stage) : 0;
+  size_t off = sizeof(Header) + sizeof(ProgRec) * progs.size();
+  std::vector<size_t> tens_off, body_off;
+  for (Program* p : progs) {
+    tens_off.push_back(off);
+    off += round_up((int64_t)(sizeof(TensRec) * p->tensors.size()), 16);
+  }
+  for (auto& s : streams) {
+    body_off.push_back(off);
+    off += sizeof(Instr) * s.size();
+  }
+  size_t total = off;
+  if (total > (size_t)kMaxImage) throw EncodeFail{DVM_E_CAPACITY, "image too large"};
+  img.assign(total, 0);
+  Header h{};
+  h.magic = kMagic;
+  h.version = kVersion;
+  h.kernel_type = kernel_type;
+  h.flags = coop ? HF_COOP : 0;
+  h.total_len = (uint32_t)total;
+  h.n_progs = (uint16_t)progs.size();
+  h.n_bind = (uint16_t)binds.size();
+  h.grid = (uint32_t)D.num_cores;
+  h.block_dim = (uint32_t)block_dim;
+  h.body_tile = (uint32_t)cdiv(block_dim, D.num_cores);
+  h.ve = (uint8_t)(progs[0]->a / 32);
+  h.n_stages = (uint8_t)n_stages;
+  h.n_slots = (uint16_t)D.n_slots;
+  h.stage_bytes = (uint32_t)stage;
+  h.hoist_bytes = (uint32_t)hoist_total;
+  std::memcpy(img.data(), &h, sizeof h);
+  uint32_t base = 0, hbase = 0;
+  for (size_t i = 0; i < progs.size(); i++) {
+    Program* p = progs[i];
+    ProgRec pr{};
+    pr.block_dim = (uint32_t)p->block_dim;
+    pr.tile_base = base;
+    pr.rank = (uint8_t)p->G.rank;
+    pr.n_tens = (uint8_t)p->tensors.size();
+    pr.kind = (uint8_t)p->kind;
+    pr.body_off = (uint32_t)body_off[i];
+    pr.body_len = (uint32_t)streams[i].size();
+    pr.tens_off = (uint32_t)tens_off[i];
+    for (int d = 0; d < 4; d++) {
+      pr.n[d] = d < p->G.rank ? (uint32_t)p->G.d[d] : 1;
+      pr.t[d] = d < p->G.rank ? (uint32_t)p->t[d] : 1;
+    }
+    pr.K = (uint32_t)p->K;
+    pr.hoist_base = hbase;
+    std::memcpy(img.data() + sizeof(Header) + i * sizeof(ProgRec), &pr, sizeof pr);
+    base += (uint32_t)p->block_dim;
+    hbase += (uint32_t)p->hoist_bytes;
+    for (size_t t = 0; t < p->tensors.size(); t++) {
+      const Tensor& tn = p->tensors[t];
+      TensRec tr{};
+      tr.dtype = (uint8_t)tn.dtype;
+      tr.binding = (uint8_t)(std::find(binds.begin(), binds.end(), tn.vid) - binds.begin());
+      for (int d = 0; d < 4; d++) tr.vs[d] = tn.vs[d];
+      std::memcpy(img.data() + tens_off[i] + t * sizeof(TensRec), &tr, sizeof tr);
+    }
+    for (size_t k = 0; k < streams[i].size(); k++) {
+      const Ins& w = streams[i][k];
+      Instr iw{};
+      iw.op = w.op;
+      iw.a = w.a;
+      iw.b = w.b;
+      iw.flags = w.flags;
+      iw.imm = w.imm;
+      iw.aux0 = w.aux0;
+      std::memcpy(img.data() + body_off[i] + k * sizeof(Instr), &iw, sizeof iw);
+    }
+  }
+  return total;
+}
+
+bool known_opcode(uint8_t op) {
+  switch (op) {
+    case OP_LD: case OP_ST: case OP_MOV: case OP_BCAST: case OP_WAIT: case OP_REL:
+    case OP_RSUM: case OP_RMAX: case OP_ASUM:
+    case OP_TILES: case OP_GSUM: case OP_JLE0: case OP_JMP: case OP_SST: case OP_END: case OP_MMA:
+      return true;
+    default:
+      return (op >= OP_SQRT && op <= OP_CASTBF) || (op >= OP_ADD && op <= OP_POW);
+  }
+}
+
+}  // namespace
+
+// =================================================================== C ABI ==
+extern "C" {
+
+static void default_desc(dvm_device_desc* d, int num_cores) {
+  d->num_cores = num_cores;
+  d->cap_elems = kCapElems;
+  d->smem_budget = 196608;
+  d->max_stages = 8;
+  d->c0_bytes = 4096;
+  d->flops_per_byte = 280;
+  d->n_slots = kNumSlots;
+}
+
+static void reserve_ctx(dvm_ctx* c) {
+  c->values.reserve(1024);
+  c->ops.reserve(1024);
+  c->groups.reserve(256);
+  c->pending.reserve(64);
+}
+
+dvm_status dvm_create(dvm_ctx** out, int cuda_device) {
+  if (!out) return DVM_E_INVALID_ARG;
+  dvm_ctx* c = new (std::nothrow) dvm_ctx();
+  if (!c) return DVM_E_INVALID_ARG;
+  char msg[200] = {0};
+  int rc = device_init(&c->dev, cuda_device, msg, sizeof msg);
+  if (rc != DVM_OK) {
+    std::snprintf(c->err, sizeof c->err, "%s", msg);
+    *out = c;  // keep the ctx so that the caller can read the reason, then destroy it
+    return rc;
+  }
+  c->has_device = true;
+  default_desc(&c->desc, c->dev.num_sms);
+  reserve_ctx(c);
+  *out = c;
+  return DVM_OK;
+}
+
+dvm_status dvm_create_host(dvm_ctx** out, const dvm_device_desc* desc) {
+  if (!out) return DVM_E_INVALID_ARG;
+  dvm_ctx* c = new (std::nothrow) dvm_ctx();
+  if (!c) return DVM_E_INVALID_ARG;
+  default_desc(&c->desc, 152);
+  if (desc) c->desc = *desc;
+  if (c->desc.n_slots != kNumSlots || c->desc.num_cores < 1 || c->desc.num_cores > kMaxGrid ||
+      c->desc.cap_elems < 512 || c->desc.cap_elems > kCapElems || c->desc.smem_budget < 4096 || c->desc.max_stages < 2 ||
+      c->desc.flops_per_byte < 1 || c->desc.c0_bytes < 0) {
+    delete c;
+    return DVM_E_INVALID_ARG;
+  }
+  reserve_ctx(c);
+  *out = c;
+  return DVM_OK;
+}
+
+void dvm_destroy(dvm_ctx* c) {
+  if (!c) return;
+  if (c->has_device) device_free(&c->dev);
+  delete c;
+}
+
+dvm_status dvm_reset(dvm_ctx* c) {
+  if (!c) return DVM_E_INVALID_ARG;
+  c->values.clear();
+  c->ops.clear();
+  c->groups.clear();
+  c->pending.clear();
+  c->launches.clear();
+  c->plan_valid.assign(c->plan_valid.size(), 0);
+  c->open = -1;
+  c->stats.host_ns_last = 0;
+  return DVM_OK;
+}
+
+dvm_status dvm_get_desc(const dvm_ctx* c, dvm_device_desc* out) {
+  if (!c || !out) return DVM_E_INVALID_ARG;
+  *out = c->desc;
+  return DVM_OK;
+}
+
+dvm_status dvm_input(dvm_ctx* c, dvm_dtype dtype, int rank, const int64_t* shape, const int64_t* strides,
+                     int32_t* out_id) {
+  if (!c || !out_id || !shape || rank < 1 || rank > 4) return DVM_E_INVALID_ARG;
+  if (dtype != DVM_F32 && dtype != DVM_BF16 && dtype != DVM_U8)
+    return c->fail(DVM_E_INVALID_ARG, "bad dtype");
+  Timer tm(c);
+  Value v;
+  v.dtype = (int8_t)dtype;
+  v.shape.rank = rank;
+  for (int d = 0; d < rank; d++) {
+    if (shape[d] < 1 || shape[d] > (int64_t)0x7fffffff) return c->fail(DVM_E_INVALID_ARG, "bad extent");
+    v.shape.d[d] = shape[d];
+  }
+  if (strides) {
+    for (int d = 0; d < rank; d++) {
+      if (strides[d] < 0) return c->fail(DVM_E_INVALID_ARG, "negative stride");
+      v.strides[d] = strides[d];
+    }
+  } else {
+    contiguous(v);
+  }
+  c->values.push_back(v);
+  *out_id = (int32_t)c->values.size() - 1;
+  return DVM_OK;
+}
+
+dvm_status dvm_graph_add(dvm_ctx* c, dvm_op opc, const int32_t* inputs, int n_inputs, const int64_t* shape,
+                         int rank, dvm_dtype out_dtype, const float* attrs, int n_attrs, int32_t* out_id) {
+  if (!c || !out_id) return DVM_E_INVALID_ARG;
+  Timer tm(c);
+  int code = (int)opc;
+  OpClass cls = op_class(code);
+  if (cls == C_BAD) return c->fail(DVM_E_UNSUPPORTED_OP, "unknown op");
+  if (out_dtype != DVM_F32 && out_dtype != DVM_BF16 && out_dtype != DVM_U8)
+    return c->fail(DVM_E_INVALID_ARG, "bad dtype");
+  const bool infer = rank == -1 && op_class(code) != C_OPQ && code != 14;
+  if (!infer && (rank < 0 || rank > 4 || (rank > 0 && !shape))) return c->fail(DVM_E_INVALID_ARG, "bad rank");
+  c->stats.ops_added++;
+  if (cls == C_OPQ) {
+    close_open(c);
+    if (rank == 0) {
+      *out_id = -1;
+      return DVM_OK;
+    }
+    return dvm_input(c, out_dtype, rank, shape, nullptr, out_id);
+  }
+  int need = is_binary(code) ? 2 : cls == C_SEL ? 3 : cls == C_MM ? 2 : 1;
+  if (n_inputs != need || !inputs) return c->fail(DVM_E_INVALID_ARG, "wrong number of inputs");
+  for (int i = 0; i < need; i++)
+    if (inputs[i] < 0 || inputs[i] >= (int32_t)c->values.size()) return c->fail(DVM_E_INVALID_ARG, "bad input id");
+  if (is_scalar(code) && (n_attrs < 1 || !attrs)) return c->fail(DVM_E_INVALID_ARG, "scalar op needs attrs[0]");
+  // infer shape
+  const Value* in0 = &c->values[inputs[0]];
+  Shape sh;
+  if (cls == C_ELT) {
+    if (is_binary(code)) {
+      if (!broadcast(in0->shape, c->values[inputs[1]].shape, &sh)) return c->fail(DVM_E_SHAPE, "not broadcastable");
+    } else if (code == 14) {
+      Shape tgt;
+      tgt.rank = rank;
+      for (int d = 0; d < rank; d++) tgt.d[d] = shape[d];
+      Shape tmp;
+      if (!broadcast(in0->shape, tgt, &tmp) || tmp != tgt) return c->fail(DVM_E_SHAPE, "bad broadcast target");
+      sh = tgt;
+    } else {
+      sh = in0->shape;
+    }
+  } else if (cls == C_RRED) {
+    sh = in0->shape;
+    sh.d[sh.rank - 1] = 1;
+  } else if (cls == C_ARED) {
+    sh.rank = 1;
+    sh.d[0] = 1;
+  } else if (cls == C_SEL) {
+    if (in0->shape.numel() != 1) return c->fail(DVM_E_SHAPE, "select predicate must have one element");
+    if (!broadcast(c->values[inputs[1]].shape, c->values[inputs[2]].shape, &sh)) return c->fail(DVM_E_SHAPE, "not broadcastable");
+  } else {  // MM
+    const Value& w = c->values[inputs[1]];
+    if (in0->shape.rank != 2 || w.shape.rank != 2 || in0->shape.d[1] != w.shape.d[0])
+      return c->fail(DVM_E_SHAPE, "matmul shapes");
+    if (in0->dtype != DVM_BF16 || w.dtype != DVM_BF16) return c->fail(DVM_E_UNSUPPORTED_OP, "matmul operands must be bf16");
+    if (in0->strides[1] != 1 || w.strides[0] != 1) return c->fail(DVM_E_UNSUPPORTED_OP, "matmul operands must be contiguous along K");
+    if ((in0->strides[0] % 8) || (w.strides[1] % 8)) return c->fail(DVM_E_UNSUPPORTED_OP, "matmul row strides must be multiples of 8");
+    sh.rank = 2;
+    sh.d[0] = in0->shape.d[0];
+    sh.d[1] = w.shape.d[1];
+  }
+  bool shape_ok = infer || rank == sh.rank;
+  for (int d = 0; shape_ok && !infer && d < rank; d++) shape_ok = shape[d] == sh.d[d];
+  if (!shape_ok) return c->fail(DVM_E_SHAPE, "given shape differs from the inferred shape");
+  if ((code == 8) != (out_dtype == DVM_U8)) return c->fail(DVM_E_UNSUPPORTED_OP, "u8 results come from isfinite only");
+  // create value + op
+  Value v;
+  v.dtype = (int8_t)out_dtype;
+  v.shape = sh;
+  contiguous(v);
+  v.producer = (int32_t)c->ops.size();
+  c->values.push_back(v);
+  int32_t vid = (int32_t)c->values.size() - 1;
+  Op op;
+  op.code = (int16_t)code;
+  op.cls = cls;
+  op.n_in = (int8_t)need;
+  for (int i = 0; i < need; i++) op.in[i] = inputs[i];
+  op.out = vid;
+  op.dtype = (int8_t)out_dtype;
+  op.n_attrs = (int8_t)std::min(n_attrs, 2);
+  for (int i = 0; i < op.n_attrs; i++) op.attrs[i] = attrs[i];
+  op.shape = sh;
+  c->ops.push_back(op);
+  int32_t oi = (int32_t)c->ops.size() - 1;
+  if (cls == C_MM) {
+    close_open(c);
+    start_group(c, PK_CUBE, sh, oi);
+  } else if (c->open >= 0 && accepts(c, c->open, oi)) {
+    append(c, c->open, oi);
+  } else {
+    Shape G = iter_shape(c, c->ops[oi]);
+    bool ok = cls != C_SEL;
+    if (ok && cls == C_RRED) {
+      int m = std::min(dtype_size(in0->dtype), dtype_size(out_dtype));
+      ok = row_fits(c, G, m);
+    }
+    if (!ok) {
+      c->ops.pop_back();
+      c->values.pop_back();
+      return c->fail(DVM_E_UNSUPPORTED_OP, cls == C_SEL ? "select outside a grid-sum group" : "row does not fit a tile");
+    }
+    close_open(c);
+    start_group(c, cls == C_ARED ? PK_SEC : PK_VEC, G, oi);
+  }
+  *out_id = vid;
+  return DVM_OK;
+}
+
+dvm_status dvm_mark_output(dvm_ctx* c, int32_t id) {
+  if (!c || id < 0 || id >= (int32_t)c->values.size()) return DVM_E_INVALID_ARG;
+  c->values[id].output = true;
+  for (size_t i = 0; i < c->plan_valid.size(); i++) c->plan_valid[i] = 0;
+  return DVM_OK;
+}
+
+dvm_status dvm_value_info(const dvm_ctx* c, int32_t id, int32_t* dtype, int32_t* rank, int64_t* shape) {
+  if (!c || id < 0 || id >= (int32_t)c->values.size()) return DVM_E_INVALID_ARG;
+  const Value& v = c->values[id];
+  if (dtype) *dtype = v.dtype;
+  if (rank) *rank = v.shape.rank;
+  if (shape)
+    for (int d = 0; d < 4; d++) shape[d] = d < v.shape.rank ? v.shape.d[d] : 1;
+  return DVM_OK;
+}
+
+dvm_status dvm_flush(dvm_ctx* c, int32_t* n_launches) {
+  if (!c || !n_launches) return DVM_E_INVALID_ARG;
+  Timer tm(c);
+  close_open(c);
+  c->plan_valid.assign(c->groups.size(), 0);
+  c->launches.clear();
+  try {
+    std::vector<int32_t> cur;
+    for (int32_t gi : c->pending) {
+      if (!cur.empty() && can_stack(c, cur, gi)) {
+        cur.push_back(gi);
+      } else {
+        if (!cur.empty()) c->launches.push_back(cur);
+        cur.assign(1, gi);
+      }
+    }
+    if (!cur.empty()) c->launches.push_back(cur);
+  } catch (const EncodeFail& f) {
+    c->pending.clear();
+    c->launches.clear();
+    return c->fail(f.code, "%s", f.why);
+  }
+  c->pending.clear();
+  c->stats.flushes++;
+  *n_launches = (int32_t)c->launches.size();
+  return DVM_OK;
+}
+
+dvm_status dvm_encode(dvm_ctx* c, int32_t launch, uint8_t* buf, size_t cap, size_t* len, int32_t* tensor_ids,
+                      int32_t* n_tensors) {
+  if (!c || !len) return DVM_E_INVALID_ARG;
+  if (launch < 0 || launch >= (int32_t)c->launches.size()) return c->fail(DVM_E_STATE, "no such launch");
+  Timer tm(c);
+  thread_local std::vector<uint8_t> img;
+  thread_local std::vector<int32_t> binds;
+  try {
+    encode_launch(c, c->launches[launch], img, binds);
+  } catch (const EncodeFail& f) {
+    return c->fail(f.code, "%s", f.why);
+  }
+  *len = img.size();
+  if (!buf || cap < img.size()) return c->fail(DVM_E_BUF_TOO_SMALL, "buffer too small");
+  std::memcpy(buf, img.data(), img.size());
+  if (tensor_ids) {
+    for (size_t i = 0; i < binds.size(); i++) tensor_ids[i] = binds[i];
+  }
+  if (n_tensors) *n_tensors = (int32_t)binds.size();
+  c->stats.launches_encoded++;
+  c->stats.programs_encoded += (int64_t)c->launches[launch].size();
+  return DVM_OK;
+}
+
+dvm_status dvm_validate(const uint8_t* img, size_t len) {
+  if (!img || len < sizeof(Header) || len > (size_t)kMaxImage) return DVM_E_BYTECODE;
+  Header h;
+  std::memcpy(&h, img, sizeof h);
+  if (h.magic != kMagic || h.version != kVersion || h.total_len != len) return DVM_E_BYTECODE;
+  if (h.kernel_type != KT_VEC && h.kernel_type != KT_CUBE) return DVM_E_BYTECODE;
+  if (h.n_progs < 1 || h.n_progs > kMaxProgs || h.n_bind < 1 || h.n_bind > kMaxBind) return DVM_E_BYTECODE;
+  if (h.grid < 1 || h.grid > (uint32_t)kMaxGrid) return DVM_E_BYTECODE;
+  if (h.ve != 4 && h.ve != 8 && h.ve != 16) return DVM_E_BYTECODE;
+  if (h.n_slots != kNumSlots) return DVM_E_BYTECODE;
+  if (sizeof(Header) + sizeof(ProgRec) * h.n_progs > len) return DVM_E_BYTECODE;
+  uint64_t bd = 0;
+  bool any_dma = false;
+  for (int p = 0; p < h.n_progs; p++) {
+    ProgRec pr;
+    std::memcpy(&pr, img + sizeof(Header) + p * sizeof(ProgRec), sizeof pr);
+    if (pr.rank < 1 || pr.rank > 4 || pr.n_tens < 1 || pr.n_tens > kMaxTens) return DVM_E_BYTECODE;
+    if (pr.body_len < 2 || pr.body_len > (uint32_t)kMaxInstr) return DVM_E_BYTECODE;
+    if ((uint64_t)pr.tens_off + sizeof(TensRec) * pr.n_tens > len) return DVM_E_BYTECODE;
+    if ((uint64_t)pr.body_off + sizeof(Instr) * pr.body_len > len) return DVM_E_BYTECODE;
+    if (pr.tens_off % 8 || pr.body_off % 16) return DVM_E_BYTECODE;
+    if (pr.tile_base != bd) return DVM_E_BYTECODE;
+    if ((h.kernel_type == KT_CUBE) != (pr.kind == PK_CUBE)) return DVM_E_BYTECODE;
+    if (pr.kind == PK_SEC && (h.n_progs != 1 || !(h.flags & HF_COOP))) return DVM_E_BYTECODE;
+    uint64_t tiles = 1;
+    for (int d = 0; d < 4; d++) {
+      if (pr.n[d] < 1 || pr.t[d] < 1) return DVM_E_BYTECODE;
+      if (d >= pr.rank && (pr.n[d] != 1 || pr.t[d] != 1)) return DVM_E_BYTECODE;
+      tiles *= (pr.n[d] + pr.t[d] - 1) / pr.t[d];
+    }
+    if (tiles != pr.block_dim) return DVM_E_BYTECODE;
+    bd += pr.block_dim;
+    if (pr.kind != PK_CUBE) {
+      uint64_t rows = 1;
+      for (int d = 0; d < pr.rank - 1; d++) rows *= pr.t[d];
+      if (pr.t[pr.rank - 1] % (32u * h.ve) || rows * pr.t[pr.rank - 1] > (uint64_t)kCapElems) return DVM_E_BYTECODE;
+    } else {
+      if (pr.rank != 2 || pr.t[0] != 128 || pr.t[1] % 16 || pr.t[1] > 256 || pr.K < 1) return DVM_E_BYTECODE;
+    }
+    TensRec tr[kMaxTens];
+    for (int t = 0; t < pr.n_tens; t++) {
+      std::memcpy(&tr[t], img + pr.tens_off + t * sizeof(TensRec), sizeof(TensRec));
+      if (tr[t].binding >= h.n_bind || tr[t].dtype < 1 || tr[t].dtype > 3) return DVM_E_BYTECODE;
+      for (int d = 0; d < 4; d++)
+        if (tr[t].vs[d] < 0) return DVM_E_BYTECODE;
+    }
+    // body: control structure + operand ranges
+    Instr w[kMaxInstr];
+    std::memcpy(w, img + pr.body_off, sizeof(Instr) * pr.body_len);
+    if (w[pr.body_len - 1].op != OP_END) return DVM_E_BYTECODE;
+    uint32_t pc = 0;
+    while (pc < pr.body_len) {
+      const Instr& x = w[pc];
+      if (!known_opcode(x.op)) return DVM_E_BYTECODE;
+      if (x.op == OP_TILES) {
+        if (pc + 1 + (uint64_t)x.imm > pr.body_len - 1) return DVM_E_BYTECODE;
+        for (uint32_t k = pc + 1; k <= pc + x.imm; k++) {
+          const Instr& y = w[k];
+          if (!known_opcode(y.op) || y.op >= OP_TILES && y.op <= OP_END) return DVM_E_BYTECODE;
+          if (y.op == OP_MMA && (pr.kind != PK_CUBE || k != pc + 1 || y.a >= pr.n_tens || y.b >= pr.n_tens)) return DVM_E_BYTECODE;
+          if (y.op == OP_LD) {
+            if (y.a > kNumSlots || y.b >= pr.n_tens) return DVM_E_BYTECODE;
+            if (y.flags & LF_DMA) {
+              if (pr.kind == PK_CUBE) return DVM_E_BYTECODE;
+              const TensRec& t = tr[y.b];
+              int esz = dtype_size(t.dtype);
+              uint64_t rows = 1;
+              for (int d = 0; d < pr.rank - 1; d++) rows *= pr.t[d];
+              uint64_t size = (((y.flags & LF_COLV) ? 1 : rows) * pr.t[pr.rank - 1] * esz + 127) / 128 * 128;
+              if (t.vs[pr.rank - 1] != 1) return DVM_E_BYTECODE;
+              if (y.flags & LF_HOIST) {
+                if (pr.hoist_base + (uint64_t)y.aux0 + size > h.hoist_bytes) return DVM_E_BYTECODE;
+              } else {
+                if ((uint64_t)y.aux0 + size > h.stage_bytes) return DVM_E_BYTECODE;
+                any_dma = true;
+              }
+            }
+          }
+          if (y.op == OP_ST && y.a >= pr.n_tens) return DVM_E_BYTECODE;
+          if (y.op == OP_MOV && (y.a > kNumSlots || y.b > kNumSlots)) return DVM_E_BYTECODE;
+          if (y.op >= OP_ADD && y.op <= OP_POW && !(y.flags & CF_IMM) && y.a > kNumSlots) return DVM_E_BYTECODE;
+          if (y.op == OP_ASUM && pr.kind != PK_SEC) return DVM_E_BYTECODE;
+        }
+        pc += 1 + x.imm;
+      } else if (x.op == OP_JLE0 || x.op == OP_JMP) {
+        int32_t off = (int32_t)x.imm;
+        int64_t tgt = (int64_t)pc + 1 + off;
+        if (pr.kind != PK_SEC || off < 0 || tgt >= pr.body_len) return DVM_E_BYTECODE;
+        pc++;
+      } else if (x.op == OP_GSUM || x.op == OP_SST) {
+        if (pr.kind != PK_SEC) return DVM_E_BYTECODE;
+        if (x.op == OP_SST && x.a >= pr.n_tens) return DVM_E_BYTECODE;
+        pc++;
+      } else if (x.op == OP_END) {
+        pc++;
+      } else {
+        return DVM_E_BYTECODE;  // tile op outside a TILES section
+      }
+    }
+  }
+  if (bd != h.block_dim) return DVM_E_BYTECODE;
+  if (h.body_tile != (h.block_dim + h.grid - 1) / h.grid) return DVM_E_BYTECODE;
+  if (any_dma && h.n_stages < 2) return DVM_E_BYTECODE;
+  if (h.kernel_type == KT_VEC && (uint64_t)h.n_stages * h.stage_bytes + h.hoist_bytes > 200 * 1024) return DVM_E_BYTECODE;
+  return DVM_OK;
+}
+
+dvm_status dvm_run(dvm_ctx* c, const uint8_t* image, size_t len, void* const* ptrs, int n, void* stream) {
+  if (!c) return DVM_E_INVALID_ARG;
+  if (!c->has_device) return c->fail(DVM_E_STATE, "encode-only context cannot run");
+  int rc = dvm_validate(image, len);
+  if (rc != DVM_OK) return c->fail(rc, "malformed launch image");
+  Header h;
+  std::memcpy(&h, image, sizeof h);
+  if (!ptrs || n != h.n_bind) return c->fail(DVM_E_INVALID_ARG, "tensor count differs from the binding table");
+  for (int i = 0; i < n; i++)
+    if (!ptrs[i] || ((uintptr_t)ptrs[i] & 15)) return c->fail(DVM_E_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
+  if (h.grid > (uint32_t)kMaxGrid) return c->fail(DVM_E_INVALID_ARG, "grid too large");
+  char msg[200] = {0};
+  rc = h.kernel_type == KT_CUBE ? cube_launch(&c->dev, image, len, ptrs, n, stream, msg, sizeof msg)
+                                : device_launch(&c->dev, image, len, ptrs, n, stream, msg, sizeof msg);
+  if (rc != DVM_OK) return c->fail(rc, "%s", msg);
+  c->stats.runs++;
+  return DVM_OK;
+}
+
+dvm_status dvm_poll_status(dvm_ctx* c, void* stream, int32_t* status) {
+  if (!c || !status) return DVM_E_INVALID_ARG;
+  if (!c->has_device) return c->fail(DVM_E_STATE, "encode-only context");
+  char msg[200] = {0};
+  int rc = device_poll(&c->dev, stream, status, msg, sizeof msg);
+  if (rc != DVM_OK) return c->fail(rc, "%s", msg);
+  return DVM_OK;
+}
+
+const char* dvm_last_error(const dvm_ctx* c) { return c ? c->err : "null context"; }
+
+dvm_status dvm_stats(const dvm_ctx* c, dvm_stats_t* out) {
+  if (!c || !out) return DVM_E_INVALID_ARG;
+  *out = c->stats;
+  return DVM_OK;
+}
+
+dvm_status dvm_stats_reset_last(dvm_ctx* c) {
+  if (!c) return DVM_E_INVALID_ARG;
+  c->stats.host_ns_last = 0;
+  return DVM_OK;
+}
+
+dvm_status dvm_debug_set_barrier(dvm_ctx* c, int skip_one_arrival, int timeout_ms) {
+  if (!c) return DVM_E_INVALID_ARG;
+  c->dev.skip_arrival = skip_one_arrival ? 1 : 0;
+  c->dev.timeout_ms = timeout_ms > 0 ? timeout_ms : 2000;
+  return DVM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// dvm_internal.h — interfaces between the host library (dvm_host.cpp) and the CUDA
+// translation units (vm_vec.cu, vm_cube.cu). Not part of the public ABI.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dvm {
+
+// Per-context device state owned by the CUDA side.
+struct DeviceState {
+  int device = -1;
+  int num_sms = 0;
+  int max_smem_optin = 0;
+  void* scratch = nullptr;        // device: [0] u64 barrier counter, [8] i32 status,
+                                  // [64..) f32 per-CTA partials (up to 1024 CTAs)
+  uint64_t barrier_base = 0;      // arrivals expected so far on the barrier counter
+  int skip_arrival = 0;           // test hook: next barrier skips one arrival
+  int timeout_ms = 2000;          // bounded waits
+  int launches = 0;
+};
+
+constexpr size_t kScratchBytes = 64 + 4 * 1024;
+constexpr int kMaxGrid = 1024;
+
+// Initialise the device state for `device` (queries SM count, allocates scratch).
+// Returns 0 or a negative DVM status; msg receives a reason on failure.
+int device_init(DeviceState* st, int device, char* msg, size_t msg_cap);
+void device_free(DeviceState* st);
+// Launch one validated image. ptrs are device pointers in binding order.
+int device_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* ptrs, int n,
+                  void* stream, char* msg, size_t msg_cap);
+// Synchronise the stream and read/clear the device status word.
+int device_poll(DeviceState* st, void* stream, int32_t* status, char* msg, size_t msg_cap);
+
+// The CUBE (matmul + epilogue) launcher, in vm_cube.cu.
+int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* ptrs, int n,
+                void* stream, char* msg, size_t msg_cap);
+
+}  // namespace dvm

@@ -1,0 +1,130 @@
+// vm_runtime.cu — device-side state of a context: scratch allocation, the launch of
+// the VEC interpreter (one of three lane widths, chosen by the header's `ve`), and the
+// status-word poll.  Cooperative launches are used for programs with a grid barrier so
+// that every CTA is resident; the barrier counter is monotonic and each launch waits
+// for its own target value, so no reset is needed between launches.
+#include <cstdio>
+#include <cstring>
+
+#include "vm_vec.cuh"
+
+namespace dvm {
+
+extern template cudaError_t launch_vec<4>(const LaunchParams&, int, size_t, bool, cudaStream_t);
+extern template cudaError_t launch_vec<8>(const LaunchParams&, int, size_t, bool, cudaStream_t);
+extern template cudaError_t launch_vec<16>(const LaunchParams&, int, size_t, bool, cudaStream_t);
+
+int device_init(DeviceState* st, int device, char* msg, size_t cap) {
+  int n = 0;
+  cudaError_t e = cudaGetDeviceCount(&n);
+  if (e != cudaSuccess || n == 0) {
+    std::snprintf(msg, cap, "no CUDA device: %s", cudaGetErrorString(e));
+    return -6;
+  }
+  if (device < 0 || device >= n) {
+    std::snprintf(msg, cap, "bad device index %d", device);
+    return -1;
+  }
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(device);
+  cudaDeviceProp prop;
+  cudaGetDeviceProperties(&prop, device);
+  if (prop.major < 10) {
+    std::snprintf(msg, cap, "device %d is sm_%d%d; this library is built for sm_103a", device, prop.major, prop.minor);
+    cudaSetDevice(prev);
+    return -6;
+  }
+  st->device = device;
+  st->num_sms = prop.multiProcessorCount;
+  st->max_smem_optin = (int)prop.sharedMemPerBlockOptin;
+  e = cudaMalloc(&st->scratch, kScratchBytes);
+  if (e == cudaSuccess) e = cudaMemset(st->scratch, 0, kScratchBytes);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    std::snprintf(msg, cap, "scratch allocation failed: %s", cudaGetErrorString(e));
+    return -6;
+  }
+  if (st->num_sms > kMaxGrid) st->num_sms = kMaxGrid;
+  return 0;
+}
+
+void device_free(DeviceState* st) {
+  if (st->scratch) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(st->device);
+    cudaFree(st->scratch);
+    cudaSetDevice(prev);
+    st->scratch = nullptr;
+  }
+}
+
+int device_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* ptrs, int n, void* stream,
+                  char* msg, size_t cap) {
+  Header h;
+  std::memcpy(&h, image, sizeof h);
+  static thread_local LaunchParams P;
+  std::memcpy(P.image, image, len);
+  for (int i = 0; i < n; i++) P.ptrs[i] = ptrs[i];
+  uint8_t* sc = static_cast<uint8_t*>(st->scratch);
+  P.barrier = reinterpret_cast<unsigned long long*>(sc);
+  P.status = reinterpret_cast<int32_t*>(sc + 8);
+  P.partials = reinterpret_cast<float*>(sc + 64);
+  P.timeout_ns = (unsigned long long)st->timeout_ms * 1000000ull;
+  P.skip_arrival = 0;
+  const bool coop = (h.flags & HF_COOP) != 0;
+  if (coop) {
+    st->barrier_base += h.grid;
+    P.barrier_target = st->barrier_base;
+    P.skip_arrival = st->skip_arrival;
+    st->skip_arrival = 0;
+  } else {
+    P.barrier_target = 0;
+  }
+  const size_t smem = kDataOff + ((h.hoist_bytes + 127) & ~127u) + (size_t)h.n_stages * h.stage_bytes;
+  if ((int)smem > st->max_smem_optin) {
+    std::snprintf(msg, cap, "launch needs %zu bytes of shared memory", smem);
+    return -8;
+  }
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (prev != st->device) cudaSetDevice(st->device);
+  cudaError_t e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (h.ve) {
+    case 4: e = launch_vec<4>(P, (int)h.grid, smem, coop, s); break;
+    case 8: e = launch_vec<8>(P, (int)h.grid, smem, coop, s); break;
+    default: e = launch_vec<16>(P, (int)h.grid, smem, coop, s); break;
+  }
+  if (prev != st->device) cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    std::snprintf(msg, cap, "launch failed: %s", cudaGetErrorString(e));
+    return -6;
+  }
+  st->launches++;
+  return 0;
+}
+
+int device_poll(DeviceState* st, void* stream, int32_t* status, char* msg, size_t cap) {
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (prev != st->device) cudaSetDevice(st->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  int32_t word = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&word, static_cast<uint8_t*>(st->scratch) + 8, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) {
+    // clear the status word and re-initialise the grid barrier
+    e = cudaMemset(st->scratch, 0, 64);
+    st->barrier_base = 0;
+  }
+  if (prev != st->device) cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    std::snprintf(msg, cap, "status read failed: %s", cudaGetErrorString(e));
+    return -6;
+  }
+  *status = word;
+  return 0;
+}
+
+}  // namespace dvm

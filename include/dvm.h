@@ -95,12 +95,12 @@ typedef enum {
 /* description of the device the encoder plans for (see dvm_create_host) */
 typedef struct {
   int32_t num_cores;      /* CTAs per launch; default: SM count */
-  int32_t cap_elems;      /* padded elements per tile; default 8192 */
+  int32_t cap_elems;      /* padded elements per tile; default 7680 */
   int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 196608 */
   int32_t max_stages;     /* default 8 */
   int32_t c0_bytes;       /* per-tile overhead of the cost model; default 4096 */
   int32_t flops_per_byte; /* cube cost-model balance; default 280 */
-  int32_t n_slots;        /* register slots besides ACC; must be 4 */
+  int32_t n_slots;        /* register slots besides ACC; must be 2 */
 } dvm_device_desc;
 
 /* counters (MindSpore summary section 3.2 flush reasons; encode latency) */
@@ -131,7 +131,8 @@ dvm_status dvm_get_desc(const dvm_ctx* ctx, dvm_device_desc* out);
 dvm_status dvm_input(dvm_ctx* ctx, dvm_dtype dtype, int rank, const int64_t* shape,
                      const int64_t* strides, int32_t* out_id);
 /* Append one op to the stream. `shape`/`rank` is the result shape (checked against
- * the inferred one; for DVM_OP_OPAQUE it is taken as given, rank 0 = no result).
+ * the inferred one; rank -1 = infer it, except for BROADCAST and OPAQUE; for
+ * DVM_OP_OPAQUE it is taken as given, rank 0 = no result).
  * `attrs` holds the scalar attributes of the scalar-form ops. *out_id = result value
  * id (-1 for an opaque op without result). */
 dvm_status dvm_graph_add(dvm_ctx* ctx, dvm_op op, const int32_t* inputs, int n_inputs,

@@ -52,8 +52,8 @@ KT_VEC, KT_CUBE = 1, 2
 MAGIC = 0x314D5644
 MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
 
-DEFAULT_DESC = dict(num_cores=152, cap_elems=8192, smem_budget=196608, max_stages=8,
-                    c0_bytes=4096, flops_per_byte=280, n_slots=4)
+DEFAULT_DESC = dict(num_cores=152, cap_elems=7680, smem_budget=196608, max_stages=8,
+                    c0_bytes=4096, flops_per_byte=280, n_slots=2)
 
 
 class EncodeError(Exception):

@@ -1,0 +1,252 @@
+"""The C-ABI library on the host (no GPU): exports, bit-exact encoding against the
+reference encoder, golden images, fusion counts and validator rejections."""
+import os
+import random
+import re
+import struct
+
+import numpy as np
+import pytest
+
+import bytecode_vm_jit_gb300 as D
+from bytecode_vm_jit_gb300 import build as B
+from bytecode_vm_jit_gb300 import workloads as W
+from oracle import ref_encoder as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    B.build()
+
+
+def test_library_exports_every_declared_symbol():
+    hdr = open(os.path.join(ROOT, "include", "dvm.h")).read()
+    declared = sorted(set(re.findall(r"\b(dvm_[a-z_]+)\s*\(", hdr)))
+    L = D.lib()
+    missing = [n for n in declared if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(declared) == set(D.EXPORTS)
+
+
+def cxx_replay(ops, inputs, outputs, desc=None):
+    """Feed an op list through the C++ library (encode-only context)."""
+    ctx = D.dvm_create_host(**(desc or {}))
+    ids = {}
+    out = []
+    try:
+        for name, (dt, shape, strides) in inputs.items():
+            ids[name] = D.dvm_input(ctx, dt, list(shape), strides)
+
+        def flush():
+            n = D.dvm_flush(ctx)
+            for i in range(n):
+                out.append(D.dvm_encode(ctx, i))
+
+        for op, ins, name, dt, attrs in ops:
+            if op == "opaque":
+                D.dvm_graph_add(ctx, "opaque", [], dt)
+                flush()
+                continue
+            ids[name] = D.dvm_graph_add(ctx, op, [ids[i] for i in ins], dt, attrs)
+            if name in outputs:
+                D.dvm_mark_output(ctx, ids[name])
+        flush()
+    finally:
+        D.dvm_destroy(ctx)
+    return out
+
+
+def ref_replay(ops, inputs, outputs, desc=None):
+    _, _, launches = R.replay(ops, inputs, outputs, desc)
+    return launches
+
+
+def same(ops, inputs, outputs, desc=None):
+    a = cxx_replay(ops, inputs, outputs, desc)
+    b = ref_replay(ops, inputs, outputs, desc)
+    assert len(a) == len(b)
+    for (ia, ba), (ib, bb) in zip(a, b):
+        assert ba == bb
+        assert ia == ib, "images differ at byte %d" % next(i for i in range(min(len(ia), len(ib))) if ia[i] != ib[i])
+        assert D.dvm_validate(ia) == 0
+    return a
+
+
+def ln_inputs(r, d=4096):
+    return {"x": ("f32", (r, d), None), "gamma": ("f32", (d,), None), "beta": ("f32", (d,), None)}
+
+
+@pytest.mark.parametrize("rows", [1, 2, 3, 17, 152, 153, 1000, 4095, 65536])
+def test_bit_exact_layernorm(rows):
+    same(W.LAYERNORM_OPS, ln_inputs(rows), W.LAYERNORM_OUT)
+
+
+@pytest.mark.parametrize("shape", [(4096, 1024), (1, 1), (7, 129), (3, 5, 130), (2, 3, 4, 257), (1000,),
+                                   (64, 64), (5, 7), (300, 8192)])
+def test_bit_exact_sqrt_add(shape):
+    same(W.SQRT_ADD_OPS, {"a": ("f32", shape, None), "b": ("f32", shape, None)}, W.SQRT_ADD_OUT)
+
+
+@pytest.mark.parametrize("t", [64, 65, 1000, 16384])
+def test_bit_exact_if_else(t):
+    same(W.IF_ELSE_ADD_OPS, {"x": ("bf16", (t, 8192), None), "z": ("bf16", (t, 8192), None)}, W.IF_ELSE_ADD_OUT)
+    same(W.IF_ELSE_PRED_OPS, {"x": ("bf16", (t, 8192), None)}, ["s"])
+
+
+@pytest.mark.parametrize("m", [1, 2, 100, 129, 324, 1000, 8192])
+def test_bit_exact_matmul(m):
+    same(W.MATMUL_ABS_OPS, {"A": ("bf16", (m, 4096), None), "W": ("bf16", (4096, 4096), [1, 4096]),
+                            "bias": ("bf16", (4096,), None)}, W.MATMUL_ABS_OUT)
+
+
+@pytest.mark.parametrize("t", [128, 129, 2112, 4096])
+def test_bit_exact_qwen(t):
+    ims = same(W.QWEN_STEP_OPS, {"x": ("bf16", (t, 5120), None), "r": ("bf16", (t, 5120), None),
+                                 "w": ("bf16", (5120,), None), "g": ("bf16", (t, 17408), None),
+                                 "u": ("bf16", (t, 17408), None)}, W.QWEN_STEP_OUT)
+    assert len(ims) == 1 and struct.unpack_from("<H", ims[0][0], 12)[0] == 2  # 2 stacked programs
+
+
+def test_bit_exact_random_streams():
+    """Random element-wise/reduce streams over random shapes and dtypes."""
+    rng = random.Random(7)
+    unary = ["sqrt", "abs", "log", "exp", "round", "floor", "neg", "rsqrt", "recip", "silu"]
+    binary = ["add", "sub", "mul", "div", "max", "min", "pow"]
+    scalar = ["adds", "subs", "muls", "divs", "maxs", "mins", "pows"]
+    for trial in range(150):
+        r = rng.randint(1, 3)
+        G = [rng.choice([1, 3, 17, 64, 255, 1000]) for _ in range(r - 1)] + [rng.choice([1, 8, 100, 128, 513, 4096])]
+        dts = ["f32", "bf16"]
+        inputs = {"x": (rng.choice(dts), tuple(G), None), "y": (rng.choice(dts), tuple(G), None),
+                  "c": (rng.choice(dts), (G[-1],), None), "rw": ("f32", tuple(G[:-1]) + (1,), None)}
+        names = ["x", "y", "c", "rw"]
+        ops = []
+        for k in range(rng.randint(1, 7)):
+            kind = rng.random()
+            out = "v%d" % k
+            dt = rng.choice(dts)
+            if kind < 0.3:
+                ops.append((rng.choice(unary), [rng.choice(names)], out, dt, ()))
+            elif kind < 0.6:
+                ops.append((rng.choice(binary), [rng.choice(names), rng.choice(names)], out, dt, ()))
+            elif kind < 0.8:
+                ops.append((rng.choice(scalar), [rng.choice(names)], out, dt, (rng.uniform(-2, 2), rng.randint(0, 1))))
+            else:
+                src = rng.choice(names)
+                ops.append((rng.choice(["reduce_sum", "reduce_max", "reduce_mean"]), [src], out, "f32", ()))
+            names.append(out)
+        outs = [o[2] for o in ops if rng.random() < 0.5] or [ops[-1][2]]
+        try:
+            ref = ref_replay(ops, inputs, outs)
+        except R.EncodeError:
+            continue
+        got = cxx_replay(ops, inputs, outs)
+        assert len(got) == len(ref), trial
+        for (ia, ba), (ib, bb) in zip(got, ref):
+            assert ba == bb and ia == ib, trial
+
+
+def test_golden_images():
+    from oracle.make_golden import CASES
+    for name, (ops, inputs, outs) in CASES.items():
+        text = open(os.path.join(ROOT, "tests", "golden", name + ".txt")).read().splitlines()
+        imgs, cur = [], None
+        for line in text:
+            if line.startswith("#"):
+                continue
+            if line.startswith("launch"):
+                cur = [bytearray(), [int(x) for x in line.split("bindings")[1].split()]]
+                imgs.append(cur)
+            else:
+                cur[0] += bytes.fromhex(line)
+        got = cxx_replay(ops, inputs, outs)
+        assert [(bytes(i), b) for i, b in imgs] == [(i, b) for i, b in got], name
+
+
+def test_encode_only_ctx_refuses_to_run():
+    ctx = D.dvm_create_host()
+    try:
+        with pytest.raises(D.DvmError):
+            D.dvm_run(ctx, b"\0" * 64, [1])
+    finally:
+        D.dvm_destroy(ctx)
+
+
+def test_shape_and_op_errors():
+    ctx = D.dvm_create_host()
+    try:
+        a = D.dvm_input(ctx, "f32", [4, 8])
+        b = D.dvm_input(ctx, "f32", [4, 9])
+        with pytest.raises(D.DvmError) as e:
+            D.dvm_graph_add(ctx, "add", [a, b], "f32")
+        assert e.value.code == -3
+        with pytest.raises(D.DvmError) as e:
+            D.dvm_graph_add(ctx, "add", [a, a], "f32", shape=[4, 7])
+        assert e.value.code == -3
+        with pytest.raises(D.DvmError) as e:
+            D.dvm_graph_add(ctx, "isfinite", [a], "f32")
+        assert e.value.code == -2
+        with pytest.raises(D.DvmError) as e:
+            D.dvm_graph_add(ctx, "add", [a, 99], "f32")
+        assert e.value.code == -1
+        with pytest.raises(D.DvmError):
+            D.dvm_encode(ctx, 0)
+        # a row that does not fit one tile cannot be reduced
+        big = D.dvm_input(ctx, "f32", [2, 100000])
+        with pytest.raises(D.DvmError) as e:
+            D.dvm_graph_add(ctx, "reduce_sum", [big], "f32")
+        assert e.value.code == -2
+    finally:
+        D.dvm_destroy(ctx)
+
+
+def _corrupt(img, off, val, fmt="<B"):
+    b = bytearray(img)
+    struct.pack_into(fmt, b, off, val)
+    return bytes(b)
+
+
+def test_validator_rejects_corrupted_images():
+    (img, _), = cxx_replay(W.LAYERNORM_OPS, ln_inputs(100), W.LAYERNORM_OUT)
+    assert D.dvm_validate(img) == 0
+    body_off = struct.unpack_from("<I", img, 48 + 12)[0]
+    tens_off = struct.unpack_from("<I", img, 48 + 20)[0]
+    bad = [
+        _corrupt(img, 0, 0x12345678, "<I"),                 # magic
+        img[:-16],                                           # truncated
+        _corrupt(img, body_off + 16 * 3, 0xEE),              # unknown opcode
+        _corrupt(img, tens_off + 1, 15),                     # binding out of range
+        _corrupt(img, 24, 99, "<I"),                         # body_tile wrong
+        _corrupt(img, 48 + 40, 3, "<I"),                     # tile extent not aligned
+    ]
+    # slot index out of range on an LD
+    for k in range(struct.unpack_from("<I", img, 48 + 16)[0]):
+        if img[body_off + 16 * k] == 0x01:
+            bad.append(_corrupt(img, body_off + 16 * k + 1, 7))
+            bad.append(_corrupt(img, body_off + 16 * k + 2, 9))  # tensor index
+            break
+    for b in bad:
+        assert D.dvm_validate(b) == -5
+
+
+def test_encode_latency_is_microseconds():
+    """In-library host time per LayerNorm instance (graph_add x9 + flush + encode)."""
+    ctx = D.dvm_create_host()
+    try:
+        rows = W.layernorm_rows()[:50]
+        per = []
+        for r in rows:
+            D.dvm_reset(ctx)
+            ids = {n: D.dvm_input(ctx, dt, list(s)) for n, (dt, s, _) in ln_inputs(r).items()}
+            for op, ins, name, dt, attrs in W.LAYERNORM_OPS:
+                ids[name] = D.dvm_graph_add(ctx, op, [ids[i] for i in ins], dt, attrs)
+            D.dvm_mark_output(ctx, ids["y"])
+            n = D.dvm_flush(ctx)
+            for i in range(n):
+                D.dvm_encode(ctx, i)
+            per.append(D.dvm_stats(ctx)["host_ns_last"] / 1e3)
+        assert np.median(per) < 200.0     # generous on a loaded CI box; bench reports the real number
+    finally:
+        D.dvm_destroy(ctx)
