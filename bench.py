@@ -1,0 +1,521 @@
+"""Benchmark of the DVM hot path on GB300: VM-interpreted fused-op HBM GB/s over
+dynamic shapes, plus host encode microseconds per op instance.
+
+Workload (default): LayerNorm over 4096, fp32, 200 dynamic instances, R = B*S rows
+with B~U{1..32}, S~U{1..2048} (seed 1).  One step = every instance fed op by op through
+the streaming fuser (dvm_graph_add), flushed, tiled and encoded (dvm_encode), and run
+by the resident interpreter (dvm_run).  Inputs are drawn once on the device from a
+seeded generator and rotated through pools larger than 4x L2, so no instance reads data
+a previous one left in L2.  `--config` selects another workload (sqrt_add,
+if_else_add, qwen_stream) for the same line format.
+
+Algorithmic bytes per instance (what a perfect fused kernel must move):
+  layernorm   32768*R + 32768          (x read, y written, gamma/beta once)
+  sqrt_add    3*4*4096*1024
+  if_else_add 65536*T (predicate pass reads x, branch pass reads x, z, writes y)
+  qwen_stream 145408*T + 10240
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "VM-interpreted fused-op HBM GB/s (% of 8 TB/s) over dynamic shapes; encode µs/op"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """Samples nvidia-smi during the timed region (SM clock, throttle reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads ----
+class Workload:
+    """Instance list + device pools + per-instance op feeding for one config."""
+
+    def __init__(self, name, rank, dev):
+        import torch
+        from bytecode_vm_jit_gb300 import workloads as W
+        self.name, self.dev, self.W = name, dev, W
+        self.torch = torch
+        seed_off = 1000 * rank
+        if name == "layernorm":
+            self.sizes = W.layernorm_rows()
+            g, b, _ = W.layernorm_params()
+            self.gamma = torch.from_numpy(g).to(dev)
+            self.beta = torch.from_numpy(b).to(dev)
+            self.pool_x = W.device_pool(4 << 30, "f32", "normal", 101 + seed_off, dev)
+            self.pool_y = torch.empty(4 << 28, dtype=torch.float32, device=dev)
+            self.d = W.LN_D
+        elif name == "sqrt_add":
+            self.sizes = [4096] * 16
+            self.pool_x = W.device_pool(1 << 30, "f32", "uniform", 100 + seed_off, dev)
+            self.pool_z = W.device_pool(1 << 30, "f32", "uniform", 200 + seed_off, dev)
+            self.pool_y = torch.empty(1 << 28, dtype=torch.float32, device=dev)
+            self.d = 1024
+        elif name == "if_else_add":
+            self.sizes = W.if_else_rows()
+            self.pool_x = W.device_pool(4 << 30, "bf16", "normal", 102 + seed_off, dev)
+            self.pool_z = W.device_pool(4 << 30, "bf16", "normal", 202 + seed_off, dev)
+            self.pool_y = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+            self.d = W.IEA_D
+        elif name == "qwen_stream":
+            self.sizes = W.qwen_tokens()[:200]
+            w, _ = W.qwen_weight()
+            self.w = W.bf16_bits_to_torch(w).to(dev)
+            self.pool_x = W.device_pool(2 << 30, "bf16", "normal", 104 + seed_off, dev)
+            self.pool_z = W.device_pool(2 << 30, "bf16", "normal", 204 + seed_off, dev)
+            self.pool_g = W.device_pool(4 << 30, "bf16", "normal", 304 + seed_off, dev)
+            self.pool_u = W.device_pool(4 << 30, "bf16", "normal", 404 + seed_off, dev)
+            self.pool_y = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+            self.pool_n = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+            self.pool_s = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+        else:
+            raise SystemExit("unknown config %s" % name)
+        self.cursor = {}
+
+    def take(self, pool, n, shape):
+        """Next n elements of a pool (rotating), viewed as `shape`."""
+        key = id(pool)
+        off = self.cursor.get(key, 0)
+        if off + n > pool.numel():
+            off = 0
+        self.cursor[key] = off + n
+        return pool[off:off + n].view(*shape)
+
+    def bytes_of(self, size):
+        if self.name == "layernorm":
+            return 32768 * size + 32768
+        if self.name == "sqrt_add":
+            return 3 * 4 * 4096 * 1024
+        if self.name == "if_else_add":
+            return 65536 * size
+        return 145408 * size + 10240
+
+    def unit_bytes(self):
+        return sum(self.bytes_of(s) for s in self.sizes)
+
+    def instance(self, i):
+        """(op list, inputs dict of device tensors, outputs dict of preallocated tensors)."""
+        W = self.W
+        s = self.sizes[i]
+        if self.name == "layernorm":
+            x = self.take(self.pool_x, s * self.d, (s, self.d))
+            y = self.take(self.pool_y, s * self.d, (s, self.d))
+            return W.LAYERNORM_OPS, {"x": x, "gamma": self.gamma, "beta": self.beta}, {"y": y}
+        if self.name == "sqrt_add":
+            a = self.take(self.pool_x, s * self.d, (s, self.d))
+            b = self.take(self.pool_z, s * self.d, (s, self.d))
+            y = self.take(self.pool_y, s * self.d, (s, self.d))
+            return W.SQRT_ADD_OPS, {"a": a, "b": b}, {"y": y}
+        if self.name == "if_else_add":
+            x = self.take(self.pool_x, s * self.d, (s, self.d))
+            z = self.take(self.pool_z, s * self.d, (s, self.d))
+            y = self.take(self.pool_y, s * self.d, (s, self.d))
+            return W.IF_ELSE_ADD_OPS, {"x": x, "z": z}, {"y": y}
+        x = self.take(self.pool_x, s * W.HIDDEN, (s, W.HIDDEN))
+        r = self.take(self.pool_z, s * W.HIDDEN, (s, W.HIDDEN))
+        g = self.take(self.pool_g, s * W.INTER, (s, W.INTER))
+        u = self.take(self.pool_u, s * W.INTER, (s, W.INTER))
+        h = self.take(self.pool_y, s * W.HIDDEN, (s, W.HIDDEN))
+        n = self.take(self.pool_n, s * W.HIDDEN, (s, W.HIDDEN))
+        so = self.take(self.pool_s, s * W.INTER, (s, W.INTER))
+        return W.QWEN_STEP_OPS, {"x": x, "r": r, "w": self.w, "g": g, "u": u}, {"h": h, "n": n, "s": so}
+
+
+class Runner:
+    """Feeds instances through the C ABI with preallocated output tensors."""
+
+    def __init__(self, dev_index):
+        import bytecode_vm_jit_gb300 as D
+        self.D = D
+        self.h = D.dvm_create(dev_index)
+        self.launches = 0
+        self.encode_ns = []      # in-library host time per instance
+        self.wall_ns = []        # Python-side host time per instance (graph_add..run)
+
+    def feed(self, ops, inputs, outputs, stream, events=None):
+        D = self.D
+        h = self.h
+        t0 = time.perf_counter_ns()
+        D.dvm_reset(h)
+        ids, tens = {}, {}
+        for name, t in inputs.items():
+            vid = D.dvm_input(h, D._dt_name(t), list(t.shape), list(t.stride()))
+            ids[name] = vid
+            tens[vid] = t
+        for op, ins, out, dt, attrs in ops:
+            if op == "opaque":
+                D.dvm_graph_add(h, "opaque", [], dt)
+                self._run_pending(tens, stream, events)
+                continue
+            vid = D.dvm_graph_add(h, op, [ids[i] for i in ins], dt, attrs)
+            ids[out] = vid
+            if out in outputs:
+                D.dvm_mark_output(h, vid)
+                tens[vid] = outputs[out]
+        self._run_pending(tens, stream, events)
+        self.encode_ns.append(D.dvm_stats(h)["host_ns_last"])
+        self.wall_ns.append(time.perf_counter_ns() - t0)
+
+    def _run_pending(self, tens, stream, events):
+        D = self.D
+        n = D.dvm_flush(self.h)
+        for i in range(n):
+            img, binds = D.dvm_encode(self.h, i)
+            ptrs = []
+            for vid in binds:
+                t = tens.get(vid)
+                if t is None:
+                    raise RuntimeError("value %d crosses launches without a buffer" % vid)
+                ptrs.append(t.data_ptr())
+            if events is not None:
+                e0 = self.torch.cuda.Event(enable_timing=True)
+                e1 = self.torch.cuda.Event(enable_timing=True)
+                e0.record()
+                D.dvm_run(self.h, img, ptrs, stream)
+                e1.record()
+                events.append((e0, e1))
+            else:
+                D.dvm_run(self.h, img, ptrs, stream)
+            self.launches += 1
+
+
+# ------------------------------------------------------------ cpu baseline --
+def cpu_baseline(name, budget_s=15.0):
+    """The oracle (numpy, fp64 evaluator) on a bounded sample of the same workload."""
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    import numpy as np
+    from bytecode_vm_jit_gb300 import workloads as W
+    from oracle.evaluator import evaluate
+    t_sum, b_sum, done = 0.0, 0, 0
+    if name == "layernorm":
+        sizes = W.layernorm_rows()
+        for i, r in enumerate(sizes):
+            inp = W.layernorm_inputs(i, r)
+            t0 = time.perf_counter()
+            evaluate(W.LAYERNORM_OPS, inp)
+            t_sum += time.perf_counter() - t0
+            b_sum += 32768 * r + 32768
+            done += 1
+            if t_sum > budget_s:
+                break
+        sample = "first %d of the 200 LayerNorm instances (rows %d..%d), full rows, in order" % (
+            done, min(sizes[:done]), max(sizes[:done]))
+    elif name == "sqrt_add":
+        inp = W.sqrt_add_inputs()
+        while t_sum < budget_s / 3:
+            t0 = time.perf_counter()
+            evaluate(W.SQRT_ADD_OPS, inp)
+            t_sum += time.perf_counter() - t0
+            b_sum += 3 * 4 * 4096 * 1024
+            done += 1
+        sample = "%d repetitions of the 4096x1024 instance" % done
+    elif name == "if_else_add":
+        sizes = W.if_else_rows()
+        for i, t in enumerate(sizes):
+            inp = W.if_else_inputs(i, t)
+            t0 = time.perf_counter()
+            evaluate(W.IF_ELSE_ADD_OPS, inp)
+            t_sum += time.perf_counter() - t0
+            b_sum += 65536 * t
+            done += 1
+            if t_sum > budget_s:
+                break
+        sample = "first %d of the 500 if-else-add instances" % done
+    else:
+        sizes = W.qwen_tokens()
+        for i, t in enumerate(sizes):
+            inp = W.qwen_inputs(i, t)
+            t0 = time.perf_counter()
+            evaluate(W.QWEN_STEP_OPS, inp)
+            t_sum += time.perf_counter() - t0
+            b_sum += 145408 * t + 10240
+            done += 1
+            if t_sum > budget_s:
+                break
+        sample = "first %d of the 2000 qwen stream steps" % done
+    cores = int(os.environ.get("OMP_NUM_THREADS", "1"))
+    return {"value": b_sum / t_sum / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds": round(t_sum, 3), "instances": done}
+
+
+# -------------------------------------------------------------- profiles ----
+def roofline_traffic(kernel_key):
+    """dram bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel_key)
+    if not ent:
+        return None, None
+    src = hashlib.sha256()
+    for fn in ent.get("sources", []):
+        with open(os.path.join(ROOT, fn), "rb") as f:
+            src.update(f.read())
+    if src.hexdigest() != ent.get("source_sha256"):
+        return None, None
+    return ent.get("dram_bytes_per_unit"), ent
+
+
+# ------------------------------------------------------------------ main ----
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dvm", choices=["dvm", "reference"])
+    ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    workload_desc = {
+        "layernorm": "LayerNorm fp32 over 4096, 200 dynamic instances R=B*S (B~U{1..32}, S~U{1..2048}, seed 1)",
+        "sqrt_add": "c = sqrt(a + b), fp32 4096x1024, single shape (16 instances per step)",
+        "if_else_add": "if-else-add bf16 [T,8192], T~U{64..16384}, 500 instances, device-side branch",
+        "qwen_stream": "Qwen3-14B-shaped stream (h=x+r, RMSNorm, silu(g)*u), first 200 of 2000 steps",
+    }[args.config]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t_all = []
+        res = None
+        for k in range(args.warmup + args.steps):
+            res = cpu_baseline(args.config, budget_s=3.0)
+            if k >= args.warmup:
+                t_all.append(res["seconds"])
+        line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.mean(t_all),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": workload_desc},
+                "cpu_baseline": {"kind": "oracle", "cores": res["cores"], "sample": res["sample"], "value": res["value"],
+                                 "unit": "GB/s"},
+                "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as dist
+    from bytecode_vm_jit_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    wl = Workload(args.config, rank, dev)
+    run = Runner(local)
+    run.torch = torch
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    n_inst = len(wl.sizes)
+
+    def step(events=None):
+        for i in range(n_inst):
+            ops, ins, outs = wl.instance(i)
+            run.feed(ops, ins, outs, sptr, events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = run.D.dvm_poll_status(run.h, sptr)
+    if st != 0:
+        raise SystemExit("device status %d after warm-up" % st)
+
+    # ---------------- timed region (device events, inputs resident in HBM)
+    run.encode_ns.clear()
+    run.wall_ns.clear()
+    launches0 = run.launches
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    gpu_launches = run.launches - launches0
+    t_local = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    ms_max = float(t_local.item())
+    units = wl.unit_bytes() * args.steps * world
+    value = units / (ms_max / 1e3) / 1e9
+    enc_us = [x / 1e3 for x in run.encode_ns]
+    wall_us = [x / 1e3 for x in run.wall_ns]
+
+    # ---------------- per-launch kernel durations for the roofline (separate pass)
+    events = []
+    step(events)
+    torch.cuda.synchronize()
+    kernel_ms = sum(a.elapsed_time(b) for a, b in events)
+    kernel_gbs = wl.unit_bytes() / (kernel_ms / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    key = {"layernorm": "vm_vec_kernel<4>", "sqrt_add": "vm_vec_kernel<4>", "if_else_add": "vm_vec_kernel<8>",
+           "qwen_stream": "vm_vec_kernel<8>"}[args.config]
+    traffic_per_unit, _ = roofline_traffic(key + ":" + args.config)
+    traffic = None
+    if traffic_per_unit is not None:
+        traffic = traffic_per_unit * wl.unit_bytes() / max(1, len(events))
+    roofline = {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak,
+                "traffic": traffic, "kernel": key, "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": wl.unit_bytes() / max(1, len(events)),
+                "avg_launch_us": 1e3 * kernel_ms / max(1, len(events)),
+                "frac_of_nominal_8tbs": kernel_gbs / NOMINAL_HBM_GBS}
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e and args.config == "layernorm":
+        e2e = e2e_layernorm(wl, run, stream, sptr)
+
+    st = run.D.dvm_poll_status(run.h, sptr)
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu:
+            cpu = cpu_baseline(args.config)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.config in ("layernorm", "sqrt_add") else "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc, "instances_per_step": n_inst,
+                       "algorithmic_bytes_per_step": wl.unit_bytes(),
+                       "l2": "inputs and outputs rotate through device pools of 4 GiB (> 4x the 129 MB L2)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
+            "frac_of_measured_hbm": value / peak,
+            "encode_us_per_instance": {"median": statistics.median(enc_us), "p99": percentile(enc_us, 99),
+                                       "source": "in-library host time (graph_add+flush+encode)"},
+            "host_us_per_instance_python": {"median": statistics.median(wall_us), "p99": percentile(wall_us, 99)},
+            "clocks": clk, "gpu_launches": gpu_launches, "device_status": st,
+            "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def percentile(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return None
+    k = min(len(xs) - 1, max(0, int(math.ceil(q / 100.0 * len(xs))) - 1))
+    return xs[k]
+
+
+def e2e_layernorm(wl, run, stream, sptr):
+    """Same metric through the C ABI with pinned host buffers: H2D of x, run, D2H of y."""
+    import torch
+    max_r = max(wl.sizes)
+    hx = torch.empty(max_r * wl.d, dtype=torch.float32, pin_memory=True)
+    hy = torch.empty(max_r * wl.d, dtype=torch.float32, pin_memory=True)
+    hx.copy_(wl.pool_x[:max_r * wl.d].cpu())
+    h2d = d2h = 0
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(len(wl.sizes)):
+        ops, ins, outs = wl.instance(i)
+        n = ins["x"].numel()
+        ins["x"].view(-1).copy_(hx[:n], non_blocking=True)
+        h2d += n * 4
+        run.feed(ops, ins, outs, sptr)
+        hy[:n].copy_(outs["y"].view(-1), non_blocking=True)
+        d2h += n * 4
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": wl.unit_bytes() / (ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    main()
