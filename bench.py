@@ -337,6 +337,8 @@ def main():
     ap.add_argument("--impl", default="dvm", choices=["dvm", "reference"])
     ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--instances", type=int, default=0, help="use only the first N instances (profiling)")
+    ap.add_argument("--fixed-size", type=int, default=0, help="override every instance's size (profiling)")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
 
@@ -387,6 +389,10 @@ def main():
         torch.cuda.synchronize()
 
     wl = Workload(args.config, rank, dev)
+    if args.instances:
+        wl.sizes = wl.sizes[:args.instances]
+    if args.fixed_size:
+        wl.sizes = [args.fixed_size] * len(wl.sizes)
     run = Runner(local)
     run.torch = torch
     stream = torch.cuda.current_stream(dev)

@@ -26,9 +26,10 @@ constexpr int kMaxTens = 16;
 constexpr int kMaxInstr = 96;
 constexpr int kMaxImage = 8192;
 constexpr int kNumSlots = 2;        // addressable register slots besides ACC
-constexpr int kVmWarps = 15;        // consumer warps of the VEC interpreter
-constexpr int kVmReg = 16;          // fp32 values per register slot per thread
-constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 7680 padded elements per tile
+constexpr int kVmWarps = 8;         // warps of the VEC interpreter
+constexpr int kVmReg = 32;          // fp32 values in ACC (and per slot) per thread
+constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 8192 padded elements per tile
+constexpr int kSmemBudget = 118784;  // DMA ring + hoist area of the VEC interpreter
 constexpr int kMaxRank = 4;
 
 enum KernelType : uint8_t { KT_VEC = 1, KT_CUBE = 2 };

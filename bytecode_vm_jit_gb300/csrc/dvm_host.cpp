@@ -728,40 +728,34 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
   const dvm_device_desc& D = c->desc;
   int r = p.G.rank;
   const int64_t* n = p.G.d;
-  int64_t al[4] = {1, 1, 1, 1};
-  al[r - 1] = p.a;
-  int64_t t[4] = {1, 1, 1, 1};
-  for (int d = 0; d < r - 1; d++) t[d] = n[d];
-  t[r - 1] = hardware_align_div(n[r - 1], 1, p.a);
-  // candidate sequence: outer -> inner shrink
-  int64_t cands[256][4];
-  int nc = 0;
-  std::memcpy(cands[nc++], t, sizeof t);
-  for (int d = 0; d < r; d++) {
-    if (d == r - 1 && rowred) break;
+  // candidate plans in spec order: inner widths largest first, each followed by the
+  // outer-to-inner shrink of the outer dims; evaluated as they are generated
+  int64_t widths[64];
+  int nw = 0;
+  widths[nw++] = hardware_align_div(n[r - 1], 1, p.a);
+  if (!rowred && widths[0] > p.a) {
     for (int64_t k = 2;; k *= 2) {
-      int64_t cc = cdiv(n[d], k);
-      int64_t nt = round_up(cc, al[d]);
-      if (nt < t[d]) {
-        t[d] = nt;
-        if (nc < 256) std::memcpy(cands[nc++], t, sizeof t);
-      }
-      if (cc <= 1 || nt <= al[d]) break;
+      int64_t cc = cdiv(n[r - 1], k);
+      int64_t nt = round_up(cc, p.a);
+      if (nt < widths[nw - 1] && nw < 64) widths[nw++] = nt;
+      if (cc <= 1 || nt <= p.a) break;
     }
   }
   LoadInfo li[kMaxTens];
-  int best = -1;
+  int64_t best_t[4] = {0, 0, 0, 0};
+  bool have = false;
   int64_t best_cost = 0;
-  for (int ci = 0; ci < nc; ci++) {
-    const int64_t* cand = cands[ci];
+  auto consider = [&](const int64_t* cand) {
+    int64_t rows = 1;
+    for (int d = 0; d < r - 1; d++) rows *= cand[d];
+    if (rows * cand[r - 1] > D.cap_elems) return;
     int64_t tiles[4] = {1, 1, 1, 1};
     for (int d = 0; d < r; d++) tiles[d] = cdiv(n[d], cand[d]);
-    int64_t rows;
-    flags_for(p, cand, tiles, li, &rows);
-    if (rows * cand[r - 1] > D.cap_elems) continue;
+    int64_t rws;
+    flags_for(p, cand, tiles, li, &rws);
     int64_t stage, hoist;
     layout(p, li, &stage, &hoist, nullptr, nullptr);
-    if (2 * stage + hoist > D.smem_budget) continue;
+    if (2 * stage + hoist > D.smem_budget) return;
     int64_t ntiles = 1;
     for (int d = 0; d < r; d++) ntiles *= tiles[d];
     int64_t waves = cdiv(ntiles, D.num_cores);
@@ -773,13 +767,31 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
       tb += dtype_size(tn.dtype) * cover;
     }
     int64_t cost = waves * (D.c0_bytes + tb);
-    if (best < 0 || cost < best_cost) {
-      best = ci;
+    if (!have || cost < best_cost) {
+      have = true;
       best_cost = cost;
+      std::memcpy(best_t, cand, sizeof best_t);
+    }
+  };
+  for (int wi = 0; wi < nw; wi++) {
+    int64_t t[4] = {1, 1, 1, 1};
+    for (int d = 0; d < r - 1; d++) t[d] = n[d];
+    t[r - 1] = widths[wi];
+    consider(t);
+    for (int d = 0; d < r - 1; d++) {
+      for (int64_t k = 2;; k *= 2) {
+        int64_t cc = cdiv(n[d], k);
+        if (cc < t[d]) {
+          t[d] = cc;
+          consider(t);
+        }
+        if (cc <= 1) break;
+      }
     }
   }
+  const int best = have ? 0 : -1;
   if (best < 0) throw EncodeFail{DVM_E_CAPACITY, "no feasible tiling"};
-  std::memcpy(p.t, cands[best], sizeof p.t);
+  std::memcpy(p.t, best_t, sizeof p.t);
   int64_t tiles[4] = {1, 1, 1, 1};
   for (int d = 0; d < r; d++) tiles[d] = cdiv(n[d], p.t[d]);
   int64_t rows;
@@ -1138,7 +1150,7 @@ extern "C" {
 static void default_desc(dvm_device_desc* d, int num_cores) {
   d->num_cores = num_cores;
   d->cap_elems = kCapElems;
-  d->smem_budget = 196608;
+  d->smem_budget = kSmemBudget;
   d->max_stages = 8;
   d->c0_bytes = 4096;
   d->flops_per_byte = 280;
@@ -1177,7 +1189,7 @@ dvm_status dvm_create_host(dvm_ctx** out, const dvm_device_desc* desc) {
   default_desc(&c->desc, 152);
   if (desc) c->desc = *desc;
   if (c->desc.n_slots != kNumSlots || c->desc.num_cores < 1 || c->desc.num_cores > kMaxGrid ||
-      c->desc.cap_elems < 512 || c->desc.cap_elems > kCapElems || c->desc.smem_budget < 4096 || c->desc.max_stages < 2 ||
+      c->desc.cap_elems < 512 || c->desc.cap_elems > kCapElems || c->desc.smem_budget < 4096 || c->desc.smem_budget > kSmemBudget || c->desc.max_stages < 2 ||
       c->desc.flops_per_byte < 1 || c->desc.c0_bytes < 0) {
     delete c;
     return DVM_E_INVALID_ARG;
@@ -1519,7 +1531,7 @@ dvm_status dvm_validate(const uint8_t* img, size_t len) {
   if (bd != h.block_dim) return DVM_E_BYTECODE;
   if (h.body_tile != (h.block_dim + h.grid - 1) / h.grid) return DVM_E_BYTECODE;
   if (any_dma && h.n_stages < 2) return DVM_E_BYTECODE;
-  if (h.kernel_type == KT_VEC && (uint64_t)h.n_stages * h.stage_bytes + h.hoist_bytes > 200 * 1024) return DVM_E_BYTECODE;
+  if (h.kernel_type == KT_VEC && (uint64_t)h.n_stages * h.stage_bytes + h.hoist_bytes > (uint64_t)kSmemBudget) return DVM_E_BYTECODE;
   return DVM_OK;
 }
 

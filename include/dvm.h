@@ -95,8 +95,8 @@ typedef enum {
 /* description of the device the encoder plans for (see dvm_create_host) */
 typedef struct {
   int32_t num_cores;      /* CTAs per launch; default: SM count */
-  int32_t cap_elems;      /* padded elements per tile; default 7680 */
-  int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 196608 */
+  int32_t cap_elems;      /* padded elements per tile; default 8192 */
+  int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 118784 */
   int32_t max_stages;     /* default 8 */
   int32_t c0_bytes;       /* per-tile overhead of the cost model; default 4096 */
   int32_t flops_per_byte; /* cube cost-model balance; default 280 */

@@ -52,7 +52,7 @@ KT_VEC, KT_CUBE = 1, 2
 MAGIC = 0x314D5644
 MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
 
-DEFAULT_DESC = dict(num_cores=152, cap_elems=7680, smem_budget=196608, max_stages=8,
+DEFAULT_DESC = dict(num_cores=152, cap_elems=8192, smem_budget=118784, max_stages=8,
                     c0_bytes=4096, flops_per_byte=280, n_slots=2)
 
 
@@ -730,28 +730,41 @@ class RefCtx:
     def plan_vec(self, prog, rowred):
         d_ = self.desc
         G, r, a = prog["G"], prog["rank"], prog["a"]
-        al = [1] * (r - 1) + [a]
-        t = list(G[:r - 1]) + [hardware_align_div(G[r - 1], 1, a)]
-        cands = [list(t)]
-        for d in range(r):
-            if d == r - 1 and rowred:
-                break
+        # inner widths, largest first
+        widths = [hardware_align_div(G[r - 1], 1, a)]
+        if not rowred and widths[0] > a:
             k = 2
             while True:
-                c = cdiv(G[d], k)
-                nt = round_up(c, al[d])
-                if nt < t[d]:
-                    t[d] = nt
-                    cands.append(list(t))
-                if c <= 1 or nt <= al[d]:
+                c = cdiv(G[r - 1], k)
+                nt = round_up(c, a)
+                if nt < widths[-1]:
+                    widths.append(nt)
+                if c <= 1 or nt <= a:
                     break
                 k *= 2
+        cands = []
+        for w in widths:
+            t = list(G[:r - 1]) + [w]
+            cands.append(list(t))
+            for d in range(r - 1):
+                k = 2
+                while True:
+                    c = cdiv(G[d], k)
+                    if c < t[d]:
+                        t[d] = c
+                        cands.append(list(t))
+                    if c <= 1:
+                        break
+                    k *= 2
         best = None
         for cand in cands:
-            tiles = [cdiv(G[d], cand[d]) for d in range(r)]
-            fl, rows = self.flags_for(prog, cand, tiles)
+            rows = 1
+            for d in range(r - 1):
+                rows *= cand[d]
             if rows * cand[r - 1] > d_["cap_elems"]:
                 continue
+            tiles = [cdiv(G[d], cand[d]) for d in range(r)]
+            fl, rows = self.flags_for(prog, cand, tiles)
             stage, hoist, _, _ = self.layout(prog, fl)
             if 2 * stage + hoist > d_["smem_budget"]:
                 continue
