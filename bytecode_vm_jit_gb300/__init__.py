@@ -28,7 +28,7 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_OP", -3: "SHAPE", -4: "BU
 EXPORTS = ["dvm_create", "dvm_create_host", "dvm_destroy", "dvm_reset", "dvm_get_desc", "dvm_input",
            "dvm_graph_add", "dvm_mark_output", "dvm_value_info", "dvm_flush", "dvm_encode",
            "dvm_validate", "dvm_run", "dvm_poll_status", "dvm_last_error", "dvm_stats",
-           "dvm_stats_reset_last", "dvm_debug_set_barrier"]
+           "dvm_stats_reset_last", "dvm_debug_set_barrier", "dvm_run_static"]
 
 MAX_IMAGE = 8192
 MAX_BIND = 16
@@ -83,6 +83,7 @@ def lib():
     L.dvm_stats.argtypes = [VP, P(Stats)]
     L.dvm_stats_reset_last.argtypes = [VP]
     L.dvm_debug_set_barrier.argtypes = [VP, ctypes.c_int, ctypes.c_int]
+    L.dvm_run_static.argtypes = [ctypes.c_char_p, ctypes.c_size_t, P(VP), ctypes.c_int, VP]
     for n in EXPORTS:
         f = getattr(L, n)
         if n not in ("dvm_destroy", "dvm_last_error"):
@@ -187,6 +188,15 @@ def dvm_run(ctx, image, ptrs, stream=None):
     n = len(ptrs)
     arr = (ctypes.c_void_p * max(1, n))(*ptrs)
     _check(ctx, lib().dvm_run(ctx, image, len(image), arr, n, stream))
+
+
+def dvm_run_static(image, ptrs, stream=None):
+    """Allocation-free launch (no context; fixed scratch inside the library)."""
+    n = len(ptrs)
+    arr = (ctypes.c_void_p * max(1, n))(*ptrs)
+    rc = lib().dvm_run_static(image, len(image), arr, n, stream)
+    if rc != 0:
+        raise DvmError(rc, "dvm_run_static")
 
 
 def dvm_poll_status(ctx, stream=None):

@@ -21,7 +21,7 @@ LIB = os.path.join(OUT, "libdvm.so")
 CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["vm_vec4.cu", "vm_vec8.cu", "vm_vec16.cu", "vm_runtime.cu", "vm_cube.cu"]
+CU_SOURCES = ["vm_vec4.cu", "vm_vec8.cu", "vm_vec16.cu", "vm_runtime.cu", "vm_cube.cu", "vm_noalloc.cu"]
 CPP_SOURCES = ["dvm_host.cpp"]
 HEADERS = ["dvm_format.h", "dvm_internal.h", "vm_common.cuh", "vm_vec.cuh"]
 

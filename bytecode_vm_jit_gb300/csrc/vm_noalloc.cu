@@ -1,0 +1,113 @@
+// vm_noalloc.cu — dvm_run_static: run a launch image without allocating anything.
+//
+// Some callers cannot call cudaMalloc at the point where they run a program: code
+// that executes inside another framework's memory arena or pool (where a stray
+// allocation would bypass its accounting or fragment it), code running under an
+// allocation budget of zero, or code that must not take the allocator's locks on a
+// latency-critical path.  dvm_run needs a context whose creation allocates a small
+// device scratch area; this entry point instead uses a fixed scratch array that lives
+// in the library image itself and is shared by every call on a device.
+//
+// The VEC interpreter needs scratch only for programs with a grid-wide sum (a grid
+// barrier counter, a status word and one partial sum per CTA); the array below holds
+// that for grids of up to kStaticMaxGrid CTAs.  The interpreter kernel is the same one
+// dvm_run launches; only the scratch pointers differ.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "vm_vec.cuh"
+#include "../../include/dvm.h"
+
+namespace dvm {
+
+extern template cudaError_t launch_vec<4>(const LaunchParams&, int, size_t, bool, cudaStream_t);
+extern template cudaError_t launch_vec<8>(const LaunchParams&, int, size_t, bool, cudaStream_t);
+extern template cudaError_t launch_vec<16>(const LaunchParams&, int, size_t, bool, cudaStream_t);
+
+// Largest grid (CTAs per launch) the fixed scratch supports, and its size:
+// [0, 8) barrier counter, [8, 12) status word, [64, 64 + 4*kStaticMaxGrid) partial sums.
+constexpr int kStaticMaxGrid = 512;
+constexpr size_t kStaticScratchBytes = 64 + 4 * kStaticMaxGrid;
+
+// The scratch array.  In host code this name is only a stand-in for the symbol; its
+// device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+struct StaticDevice {
+  bool ready = false;
+  void* scratch = nullptr;  // device address of g_static_scratch on this device
+  int num_sms = 0;
+  int max_smem_optin = 0;
+};
+StaticDevice g_devices[kMaxDevices];
+std::mutex g_setup_mutex;
+}  // namespace
+
+}  // namespace dvm
+
+using namespace dvm;
+
+extern "C" int32_t dvm_run_static(const uint8_t* image, size_t len, void* const* tensor_ptrs, int n_tensors,
+                                  void* stream) {
+  if (dvm_validate(image, len) != 0) return -5;  // DVM_E_BYTECODE
+  Header h;
+  std::memcpy(&h, image, sizeof h);
+  if (h.kernel_type != KT_VEC) return -2;              // DVM_E_UNSUPPORTED_OP: VEC programs only
+  if (h.grid > (uint32_t)kStaticMaxGrid) return -8;    // DVM_E_CAPACITY: grid beyond the fixed scratch
+  if (!tensor_ptrs || n_tensors != h.n_bind) return -1;
+  for (int i = 0; i < n_tensors; i++)
+    if (!tensor_ptrs[i] || ((uintptr_t)tensor_ptrs[i] & 15)) return -1;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -6;
+  StaticDevice& D = g_devices[dev];
+  if (!D.ready) {
+    // one-time set-up for this device (the device is current here)
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!D.ready) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return -6;
+      int sms = 0, smem = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -6;
+      if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return -6;
+      if (cudaMemset(ptr, 0, kStaticScratchBytes) != cudaSuccess) return -6;
+      D.scratch = ptr;
+      D.num_sms = sms;
+      D.max_smem_optin = smem;
+      D.ready = true;
+    }
+  }
+  const size_t smem = kDataOff + ((h.hoist_bytes + 127) & ~127u) + (size_t)h.n_stages * h.stage_bytes;
+  if ((int)smem > D.max_smem_optin) return -8;
+
+  static thread_local LaunchParams P;
+  std::memcpy(P.image, image, len);
+  for (int i = 0; i < n_tensors; i++) P.ptrs[i] = tensor_ptrs[i];
+  uint8_t* sc = static_cast<uint8_t*>(D.scratch);
+  P.barrier = reinterpret_cast<unsigned long long*>(sc);
+  P.status = reinterpret_cast<int32_t*>(sc + 8);
+  P.partials = reinterpret_cast<float*>(sc + 64);
+  P.timeout_ns = 2000ull * 1000000ull;
+  P.skip_arrival = 0;
+  const bool coop = (h.flags & HF_COOP) != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (coop) {
+    // the barrier counter and status word must start at zero for this launch
+    if (cudaMemsetAsync(sc, 0, 64, s) != cudaSuccess) return -6;
+    P.barrier_target = h.grid;
+  } else {
+    P.barrier_target = 0;
+  }
+  cudaError_t e;
+  switch (h.ve) {
+    case 4: e = launch_vec<4>(P, (int)h.grid, smem, coop, s); break;
+    case 8: e = launch_vec<8>(P, (int)h.grid, smem, coop, s); break;
+    default: e = launch_vec<16>(P, (int)h.grid, smem, coop, s); break;
+  }
+  return e == cudaSuccess ? 0 : -6;
+}

@@ -167,6 +167,29 @@ const char* dvm_last_error(const dvm_ctx* ctx);
 dvm_status dvm_stats(const dvm_ctx* ctx, dvm_stats_t* out);
 dvm_status dvm_stats_reset_last(dvm_ctx* ctx);
 
+/* Allocation-free variant of dvm_run.  The DVM pages have no counterpart: this exists
+ * for callers that cannot call cudaMalloc when they run a program — code living inside
+ * another framework's memory pool or arena (an outside allocation would escape its
+ * accounting), code under a zero allocation budget, or latency-critical paths that must
+ * not take the allocator's locks.  dvm_run needs a context whose creation allocates
+ * device scratch; this call needs no context and allocates nothing: it runs the same
+ * VEC interpreter with its scratch (grid-barrier counter, status word, per-CTA partial
+ * sums) in a fixed array of 2112 bytes compiled into the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   - image/len: a launch image from dvm_encode (VEC kernel type only; a CUBE image
+ *     returns DVM_E_UNSUPPORTED_OP).  Images whose grid exceeds 512 CTAs return
+ *     DVM_E_CAPACITY.  Other checks and errors as dvm_run.
+ *   - tensor_ptrs/n_tensors: device pointers in binding order, 16-byte aligned; the
+ *     caller owns all of them.  stream: a cudaStream_t (NULL = legacy default stream).
+ *   - The first call on a device (the device current at the call) looks up the array's
+ *     device address and zeroes it; make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents;
+ *     the parts that must start at zero are cleared on the stream before each launch
+ *     that uses them.  Calls that overlap on the GPU (e.g. on two streams) race on it.
+ *   - Device-side status (a barrier timeout) is not reported by this path. */
+dvm_status dvm_run_static(const uint8_t* image, size_t len, void* const* tensor_ptrs, int n_tensors,
+                          void* stream);
+
 /* Test hook: make the next grid barrier of `ctx` skip one CTA's arrival so that the
  * bounded wait expires (checks the timeout path; never hangs: the wait is limited to
  * about `timeout_ms` milliseconds). timeout_ms <= 0 restores the default (2000). */

@@ -1,0 +1,97 @@
+"""The allocation-free entry point dvm_run_static against dvm_run (GPU).
+
+dvm_run_static serves callers that cannot allocate device memory when they run a
+program (code inside another framework's memory pool, under a zero allocation budget,
+or on a path that must not take allocator locks).  It runs the same interpreter with
+its scratch in a fixed array inside the library.  This file is collected last so that
+a failure here cannot hide failures elsewhere; it also passes alone in a fresh process.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bytecode_vm_jit_gb300 as D
+from bytecode_vm_jit_gb300 import workloads as W
+from oracle.bf16 import bf16_bits_to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bytecode_vm_jit_gb300 import build as B
+    B.build()
+    torch.cuda.set_device(0)
+
+
+def encode(ops, inputs, outputs):
+    """Encode with an encode-only context; returns [(image, binding value ids)], id map."""
+    ctx = D.dvm_create_host(num_cores=torch.cuda.get_device_properties(0).multi_processor_count)
+    ids = {}
+    for name, t in inputs.items():
+        ids[name] = D.dvm_input(ctx, D._dt_name(t), list(t.shape), list(t.stride()))
+    for op, ins, out, dt, attrs in ops:
+        ids[out] = D.dvm_graph_add(ctx, op, [ids[i] for i in ins], dt, attrs)
+        if out in outputs:
+            D.dvm_mark_output(ctx, ids[out])
+    launches = [D.dvm_encode(ctx, i) for i in range(D.dvm_flush(ctx))]
+    shapes = {vid: D.dvm_value_info(ctx, vid) for _, b in launches for vid in b}
+    D.dvm_destroy(ctx)
+    return launches, ids, shapes
+
+
+def run_static(ops, inputs, outputs):
+    launches, ids, shapes = encode(ops, inputs, outputs)
+    bufs = {ids[n]: t for n, t in inputs.items()}
+    for img, binds in launches:
+        for vid in binds:
+            if vid not in bufs:
+                dt, shape = shapes[vid]
+                bufs[vid] = torch.empty(shape, dtype={1: torch.float32, 2: torch.bfloat16, 3: torch.uint8}[dt],
+                                        device="cuda")
+        D.dvm_run_static(img, [bufs[v].data_ptr() for v in binds], torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return {n: bufs[ids[n]] for n in outputs}
+
+
+def as_f64(t):
+    if t.dtype == torch.bfloat16:
+        return bf16_bits_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))
+    return t.cpu().numpy().astype(np.float64)
+
+
+def test_static_path_matches_dvm_run_twice():
+    # if-else-add uses the grid barrier and per-CTA partial sums (the scratch)
+    for i in (0, 1):
+        inp = W.if_else_inputs(i, 333)
+        dev = {k: W.bf16_bits_to_torch(a).cuda() for k, (a, _) in inp.items()}
+        ref = as_f64(D.run_ops(W.IF_ELSE_ADD_OPS, dev, W.IF_ELSE_ADD_OUT)["y"])
+        for _ in range(2):   # two calls in a row share the fixed scratch
+            got = as_f64(run_static(W.IF_ELSE_ADD_OPS, dev, W.IF_ELSE_ADD_OUT)["y"])
+            assert np.array_equal(got, ref)
+    # a program without a grid barrier, fp32 tolerance of the tests
+    inp = W.layernorm_inputs(0, 300)
+    dev = {k: torch.from_numpy(a).cuda() for k, (a, _) in inp.items()}
+    ref = as_f64(D.run_ops(W.LAYERNORM_OPS, dev, W.LAYERNORM_OUT)["y"])
+    for _ in range(2):
+        got = as_f64(run_static(W.LAYERNORM_OPS, dev, W.LAYERNORM_OUT)["y"])
+        assert np.all(np.abs(got - ref) <= 1e-4 * np.maximum(1.0, np.abs(ref)))
+
+
+def test_static_path_rejects_oversized_grid():
+    """A valid image planned for 1024 CTAs exceeds the fixed scratch (512 CTAs)."""
+    inp = W.if_else_inputs(0, 64)
+    dev = {k: W.bf16_bits_to_torch(a).cuda() for k, (a, _) in inp.items()}
+    ctx = D.dvm_create_host(num_cores=1024)
+    ids = {n: D.dvm_input(ctx, "bf16", list(t.shape)) for n, t in dev.items()}
+    for op, ins, out, dt, attrs in W.IF_ELSE_ADD_OPS:
+        ids[out] = D.dvm_graph_add(ctx, op, [ids[i] for i in ins], dt, attrs)
+    D.dvm_mark_output(ctx, ids["y"])
+    D.dvm_flush(ctx)
+    img, binds = D.dvm_encode(ctx, 0)
+    D.dvm_destroy(ctx)
+    assert D.dvm_validate(img) == 0
+    y = torch.empty_like(dev["x"])
+    with pytest.raises(D.DvmError) as e:
+        D.dvm_run_static(img, [dev["x"].data_ptr(), dev["z"].data_ptr(), y.data_ptr()])
+    assert e.value.code == -8
