@@ -1055,7 +1055,7 @@ size_t encode_launch(dvm_ctx* c, const std::vector<int32_t>& launch, std::vector
     block_dim += p->block_dim;
   }
   int64_t n_stages;
-  if (kernel_type == KT_CUBE) n_stages = std::min<int64_t>(D.max_stages, D.smem_budget / stage);
+  if (kernel_type == KT_CUBE) n_stages = std::min<int64_t>(D.max_stages, kCubeRingBytes / stage);
   else n_stages = stage ? std::min<int64_t>(D.max_stages, (D.smem_budget - hoist_total) / stage) : 0;
   size_t off = sizeof(Header) + sizeof(ProgRec) * progs.size();
   std::vector<size_t> tens_off, body_off;
@@ -1466,6 +1466,10 @@ dvm_status dvm_validate(const uint8_t* img, size_t len) {
       if (pr.t[pr.rank - 1] % (32u * h.ve) || rows * pr.t[pr.rank - 1] > (uint64_t)kCapElems) return DVM_E_BYTECODE;
     } else {
       if (pr.rank != 2 || pr.t[0] != 128 || pr.t[1] % 16 || pr.t[1] > 256 || pr.K < 1) return DVM_E_BYTECODE;
+      // one MatMul program per launch; its TMA ring: stages of A [128 x 64] + W [t_N x 64] bf16
+      if (h.n_progs != 1 || h.n_stages < 2 || h.n_stages > 8) return DVM_E_BYTECODE;
+      if (h.stage_bytes != (128 + pr.t[1]) * 128 || (uint64_t)h.n_stages * h.stage_bytes > (uint64_t)kCubeRingBytes)
+        return DVM_E_BYTECODE;
     }
     TensRec tr[kMaxTens];
     for (int t = 0; t < pr.n_tens; t++) {
@@ -1478,6 +1482,22 @@ dvm_status dvm_validate(const uint8_t* img, size_t len) {
     Instr w[kMaxInstr];
     std::memcpy(w, img + pr.body_off, sizeof(Instr) * pr.body_len);
     if (w[pr.body_len - 1].op != OP_END) return DVM_E_BYTECODE;
+    if (pr.kind == PK_CUBE) {
+      // TILES, MMA A W, element-wise epilogue words, END; operands bf16 and K-contiguous
+      if (pr.body_len < 3 || w[0].op != OP_TILES || w[0].imm + 2 != pr.body_len || w[1].op != OP_MMA) return DVM_E_BYTECODE;
+      if (w[1].a >= pr.n_tens || w[1].b >= pr.n_tens) return DVM_E_BYTECODE;
+      const TensRec& A = tr[w[1].a];
+      const TensRec& W = tr[w[1].b];
+      if (A.dtype != DT_BF16 || W.dtype != DT_BF16 || A.vs[1] != 1 || W.vs[0] != 1) return DVM_E_BYTECODE;
+      if ((pr.n[0] > 1 && (A.vs[0] == 0 || A.vs[0] % 8)) || (pr.n[1] > 1 && (W.vs[1] == 0 || W.vs[1] % 8))) return DVM_E_BYTECODE;
+      for (uint32_t k = 2; k + 1 < pr.body_len; k++) {
+        const Instr& y = w[k];
+        const bool elt = y.op == OP_LD || y.op == OP_ST || y.op == OP_MOV || y.op == OP_BCAST ||
+                         (y.op >= OP_SQRT && y.op <= OP_CASTBF) || (y.op >= OP_ADD && y.op <= OP_POW);
+        if (!elt || (y.op == OP_LD && (y.flags & ~LF_ROWV))) return DVM_E_BYTECODE;
+        if (y.op == OP_ST && pr.n[1] > 1 && tr[y.a < pr.n_tens ? y.a : 0].vs[1] == 0) return DVM_E_BYTECODE;
+      }
+    }
     uint32_t pc = 0;
     while (pc < pr.body_len) {
       const Instr& x = w[pc];

@@ -51,6 +51,7 @@ VEC, SEC, CUBE = 0, 1, 2
 KT_VEC, KT_CUBE = 1, 2
 MAGIC = 0x314D5644
 MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
+CUBE_RING_BYTES = 196608   # shared-memory ring of the MatMul tile op (A and W k-blocks)
 
 DEFAULT_DESC = dict(num_cores=152, cap_elems=8192, smem_budget=118784, max_stages=8,
                     c0_bytes=4096, flops_per_byte=280, n_slots=2)
@@ -896,7 +897,7 @@ class RefCtx:
         stage = max(p["stage_bytes"] for p in progs)
         hoist_total = sum(p["hoist_bytes"] for p in progs)
         if kernel_type == KT_CUBE:
-            n_stages = min(d_["max_stages"], d_["smem_budget"] // stage)
+            n_stages = min(d_["max_stages"], CUBE_RING_BYTES // stage)
         else:
             n_stages = min(d_["max_stages"], (d_["smem_budget"] - hoist_total) // stage) if stage else 0
         # offsets
