@@ -7,13 +7,15 @@ the streaming fuser (dvm_graph_add), flushed, tiled and encoded (dvm_encode), an
 by the resident interpreter (dvm_run).  Inputs are drawn once on the device from a
 seeded generator and rotated through pools larger than 4x L2, so no instance reads data
 a previous one left in L2.  `--config` selects another workload (sqrt_add,
-if_else_add, qwen_stream) for the same line format.
+if_else_add, qwen_stream, matmul) for the same line format; matmul reports tensor
+TFLOP/s of the CUBE kernel (MatMul tile op + Abs(x+bias)*0.5 epilogue).
 
 Algorithmic bytes per instance (what a perfect fused kernel must move):
   layernorm   32768*R + 32768          (x read, y written, gamma/beta once)
   sqrt_add    3*4*4096*1024
   if_else_add 65536*T (predicate pass reads x, branch pass reads x, z, writes y)
   qwen_stream 145408*T + 10240
+  matmul      2*M*4096*4096 flops (reported in TFLOP/s); bytes 16384*M + 33554432 + 8192
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -30,8 +32,13 @@ import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+# The oracle baseline is timed single-threaded; BLAS and OpenMP read these when numpy
+# first loads, so they are fixed here, before any import that loads numpy.
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("OPENBLAS_NUM_THREADS", os.environ["OMP_NUM_THREADS"])
 
 METRIC = "VM-interpreted fused-op HBM GB/s (% of 8 TB/s) over dynamic shapes; encode µs/op"
+METRIC_MM = "VM-interpreted MatMul+Elemwise tensor TFLOP/s over dynamic shapes; encode µs/op"
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -42,6 +49,16 @@ def load_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def load_tensor_peaks():
+    """(burst, sustained) dense bf16 TFLOP/s and their source."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 1900.0, 1700.0, "fallback"
 
 
 # ------------------------------------------------------------------ clocks --
@@ -138,6 +155,13 @@ class Workload:
             self.pool_y = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
             self.pool_n = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
             self.pool_s = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+        elif name == "matmul":
+            self.sizes = W.matmul_rows()
+            wt, bias, _ = W.matmul_params()
+            self.wt = W.bf16_bits_to_torch(wt).to(dev)            # Wt[N,K]; W = Wt.t()
+            self.bias = W.bf16_bits_to_torch(bias).to(dev)
+            self.pool_x = W.device_pool(4 << 30, "bf16", "normal", 103 + seed_off, dev, std=0.02)
+            self.pool_y = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
         else:
             raise SystemExit("unknown config %s" % name)
         self.cursor = {}
@@ -158,7 +182,12 @@ class Workload:
             return 3 * 4 * 4096 * 1024
         if self.name == "if_else_add":
             return 65536 * size
+        if self.name == "matmul":
+            return 16384 * size + 33554432 + 8192
         return 145408 * size + 10240
+
+    def flops_of(self, size):
+        return 2 * size * self.W.MM_N * self.W.MM_K if self.name == "matmul" else 0
 
     def unit_bytes(self):
         return sum(self.bytes_of(s) for s in self.sizes)
@@ -181,6 +210,10 @@ class Workload:
             z = self.take(self.pool_z, s * self.d, (s, self.d))
             y = self.take(self.pool_y, s * self.d, (s, self.d))
             return W.IF_ELSE_ADD_OPS, {"x": x, "z": z}, {"y": y}
+        if self.name == "matmul":
+            a = self.take(self.pool_x, s * W.MM_K, (s, W.MM_K))
+            y = self.take(self.pool_y, s * W.MM_N, (s, W.MM_N))
+            return W.MATMUL_ABS_OPS, {"A": a, "W": self.wt.t(), "bias": self.bias}, {"y": y}
         x = self.take(self.pool_x, s * W.HIDDEN, (s, W.HIDDEN))
         r = self.take(self.pool_z, s * W.HIDDEN, (s, W.HIDDEN))
         g = self.take(self.pool_g, s * W.INTER, (s, W.INTER))
@@ -252,7 +285,6 @@ class Runner:
 # ------------------------------------------------------------ cpu baseline --
 def cpu_baseline(name, budget_s=15.0):
     """The oracle (numpy, fp64 evaluator) on a bounded sample of the same workload."""
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
     import numpy as np
     from bytecode_vm_jit_gb300 import workloads as W
     from oracle.evaluator import evaluate
@@ -291,6 +323,25 @@ def cpu_baseline(name, budget_s=15.0):
             if t_sum > budget_s:
                 break
         sample = "first %d of the 500 if-else-add instances" % done
+    elif name == "matmul":
+        sizes = W.matmul_rows()
+        wt, bias, _ = W.matmul_params()
+        f_sum = 0
+        for i, m in enumerate(sizes):
+            inp = W.matmul_inputs(i, m, small_params=(wt, bias))
+            inp = {"A": inp["A"], "W": (np.ascontiguousarray(wt.T), "bf16"), "bias": inp["bias"]}
+            t0 = time.perf_counter()
+            evaluate(W.MATMUL_ABS_OPS, inp)
+            t_sum += time.perf_counter() - t0
+            f_sum += 2 * m * W.MM_N * W.MM_K
+            done += 1
+            if t_sum > budget_s:
+                break
+        cores = int(os.environ.get("OMP_NUM_THREADS", "1"))
+        return {"value": f_sum / t_sum / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": "first %d of the 100 MatMul+Abs instances (M %d..%d), fp64 numpy matmul" % (
+                    done, min(sizes[:done]), max(sizes[:done])),
+                "seconds": round(t_sum, 3), "instances": done}
     else:
         sizes = W.qwen_tokens()
         for i, t in enumerate(sizes):
@@ -335,7 +386,7 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dvm", choices=["dvm", "reference"])
-    ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream"])
+    ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream", "matmul"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--instances", type=int, default=0, help="use only the first N instances (profiling)")
     ap.add_argument("--fixed-size", type=int, default=0, help="override every instance's size (profiling)")
@@ -353,7 +404,12 @@ def main():
         "sqrt_add": "c = sqrt(a + b), fp32 4096x1024, single shape (16 instances per step)",
         "if_else_add": "if-else-add bf16 [T,8192], T~U{64..16384}, 500 instances, device-side branch",
         "qwen_stream": "Qwen3-14B-shaped stream (h=x+r, RMSNorm, silu(g)*u), first 200 of 2000 steps",
+        "matmul": "y = Abs(A@W + bias)*0.5, bf16 in / fp32 acc / bf16 out, A[M,4096], W[4096,4096], "
+                  "M log-uniform in [1,8192], 100 instances (seed 3)",
     }[args.config]
+    is_mm = args.config == "matmul"
+    metric = METRIC_MM if is_mm else METRIC
+    unit = "TFLOP/s" if is_mm else "GB/s"
 
     if args.impl == "reference":
         if rank != 0:
@@ -364,13 +420,13 @@ def main():
             res = cpu_baseline(args.config, budget_s=3.0)
             if k >= args.warmup:
                 t_all.append(res["seconds"])
-        line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": args.gpus,
+        line = {"impl": "reference", "metric": metric, "value": res["value"], "unit": unit, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.mean(t_all),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": {"workload": workload_desc},
                 "cpu_baseline": {"kind": "oracle", "cores": res["cores"], "sample": res["sample"], "value": res["value"],
-                                 "unit": "GB/s"},
-                "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                                 "unit": unit},
+                "e2e": {"value": res["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
@@ -432,8 +488,12 @@ def main():
     if world > 1:
         dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
     ms_max = float(t_local.item())
-    units = wl.unit_bytes() * args.steps * world
-    value = units / (ms_max / 1e3) / 1e9
+    if is_mm:
+        units = sum(wl.flops_of(m) for m in wl.sizes) * args.steps * world
+        value = units / (ms_max / 1e3) / 1e12
+    else:
+        units = wl.unit_bytes() * args.steps * world
+        value = units / (ms_max / 1e3) / 1e9
     enc_us = [x / 1e3 for x in run.encode_ns]
     wall_us = [x / 1e3 for x in run.wall_ns]
 
@@ -445,16 +505,32 @@ def main():
     kernel_gbs = wl.unit_bytes() / (kernel_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
     key = {"layernorm": "vm_vec_kernel<4>", "sqrt_add": "vm_vec_kernel<4>", "if_else_add": "vm_vec_kernel<8>",
-           "qwen_stream": "vm_vec_kernel<8>"}[args.config]
+           "qwen_stream": "vm_vec_kernel<8>", "matmul": "vm_cube_kernel"}[args.config]
     traffic_per_unit, _ = roofline_traffic(key + ":" + args.config)
     traffic = None
     if traffic_per_unit is not None:
         traffic = traffic_per_unit * wl.unit_bytes() / max(1, len(events))
-    roofline = {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak,
-                "traffic": traffic, "kernel": key, "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": wl.unit_bytes() / max(1, len(events)),
-                "avg_launch_us": 1e3 * kernel_ms / max(1, len(events)),
-                "frac_of_nominal_8tbs": kernel_gbs / NOMINAL_HBM_GBS}
+    if is_mm:
+        burst, sustained, tsrc = load_tensor_peaks()
+        per = [a.elapsed_time(b) for a, b in events]           # one CUBE launch per instance
+        flops = [wl.flops_of(m) for m in wl.sizes]
+        big = [i for i, m in enumerate(wl.sizes) if m >= 1024]
+        tf = sum(flops) / (kernel_ms / 1e3) / 1e12
+        tf_big = sum(flops[i] for i in big) / (sum(per[i] for i in big) / 1e3) / 1e12 if big else None
+        roofline = {"bound": "tensor", "achieved": tf, "peak": burst, "unit": "TFLOP/s", "frac": tf / burst,
+                    "traffic": traffic, "kernel": key, "peak_source": tsrc + " (burst)",
+                    "frac_of_sustained": tf / sustained,
+                    "large_m": {"m_min": 1024, "instances": len(big), "achieved": tf_big,
+                                "frac": tf_big / burst if tf_big else None},
+                    "algorithmic_flops_per_launch": sum(flops) / max(1, len(events)),
+                    "avg_launch_us": 1e3 * kernel_ms / max(1, len(events)),
+                    "hbm_gbs_algorithmic": kernel_gbs}
+    else:
+        roofline = {"bound": "hbm", "achieved": kernel_gbs, "peak": peak, "unit": "GB/s", "frac": kernel_gbs / peak,
+                    "traffic": traffic, "kernel": key, "peak_source": peak_kind,
+                    "algorithmic_bytes_per_launch": wl.unit_bytes() / max(1, len(events)),
+                    "avg_launch_us": 1e3 * kernel_ms / max(1, len(events)),
+                    "frac_of_nominal_8tbs": kernel_gbs / NOMINAL_HBM_GBS}
 
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
@@ -467,16 +543,17 @@ def main():
         if world == 1 and not args.no_cpu:
             cpu = cpu_baseline(args.config)
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.config in ("layernorm", "sqrt_add") else "bf16",
             "data": "synthetic",
             "config": {"workload": workload_desc, "instances_per_step": n_inst,
                        "algorithmic_bytes_per_step": wl.unit_bytes(),
-                       "l2": "inputs and outputs rotate through device pools of 4 GiB (> 4x the 129 MB L2)",
+                       "l2": "inputs and outputs rotate through device pools of 1-4 GiB (> 4x the 129 MB L2)"
+                             + ("; W (32 MiB) stays resident, as the weights of a layer do" if is_mm else ""),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "pct_of_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
-            "frac_of_measured_hbm": value / peak,
+            "pct_of_8tbs": None if is_mm else 100.0 * value / NOMINAL_HBM_GBS,
+            "frac_of_measured_hbm": None if is_mm else value / peak,
             "encode_us_per_instance": {"median": statistics.median(enc_us), "p99": percentile(enc_us, 99),
                                        "source": "in-library host time (graph_add+flush+encode)"},
             "host_us_per_instance_python": {"median": statistics.median(wall_us), "p99": percentile(wall_us, 99)},

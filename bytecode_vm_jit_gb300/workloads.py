@@ -231,8 +231,9 @@ def qwen_inputs(i, t, seed=4, hidden=HIDDEN, inter=INTER):
 # --------------------------------------------------------------------------
 # device pools for the benchmark (torch, seeded; values are N(0,1) or U[0,1))
 # --------------------------------------------------------------------------
-def device_pool(nbytes, dtype, dist, seed, device="cuda"):
-    """A flat device tensor of about `nbytes` bytes drawn from a seeded generator."""
+def device_pool(nbytes, dtype, dist, seed, device="cuda", std=1.0):
+    """A flat device tensor of about `nbytes` bytes drawn from a seeded generator
+    (normal draws are scaled by `std` in fp32 before the cast)."""
     import torch
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
     esz = 4 if dtype == "f32" else 2
@@ -244,7 +245,7 @@ def device_pool(nbytes, dtype, dist, seed, device="cuda"):
     for o in range(0, n, chunk):
         m = min(chunk, n - o)
         if dist == "normal":
-            out[o:o + m] = torch.randn(m, generator=g, device=device, dtype=torch.float32).to(tdt)
+            out[o:o + m] = (torch.randn(m, generator=g, device=device, dtype=torch.float32) * std).to(tdt)
         else:
             out[o:o + m] = torch.rand(m, generator=g, device=device, dtype=torch.float32).to(tdt)
     return out
