@@ -3,22 +3,28 @@
 //
 // Execution model (DVM review page, section 4.4 "virtual machine execution"): each CTA
 // is one "AI core"; it computes its contiguous tile range [c*body_tile,
-// min((c+1)*body_tile, block_dim)) and, for each tile, decodes the code body and calls
+// min((c+1)*body_tile, block_dim)) and, for each tile, decodes the code body and runs
 // the matching virtual-instruction function.  Decoding is warp-uniform from the image
 // staged in shared memory.  Section 3.2's asynchronous flows map onto one CTA:
-//   * DMA flow    -> thread 0 keeps a ring of shared-memory stages filled S-1 tiles
-//                    ahead with cp.async.bulk copies, signalled by mbarriers;
-//   * vector flow -> 8 warps move a tile from its stage into registers (LD), run the
-//                    element-wise chain in registers, reduce rows with warp shuffles,
-//                    and store from registers straight to HBM (ST);
+//   * DMA flow    -> thread 0 keeps a ring of shared-memory stages filled ahead with
+//                    cp.async.bulk copies, completion counted on mbarriers; it tops the
+//                    ring up without blocking and waits only when the ring runs dry;
+//   * vector flow -> the 8 warps move a tile from its stage into registers (LD),
+//                    run the element-wise chain in registers, reduce rows with warp
+//                    shuffles, and store from registers straight to HBM (ST);
 //   * the WAIT / REL words the encoder inserts are the syncs between the two flows.
 //
-// Registers follow an accumulator machine: ACC (REG = 32 fp32 values per thread in
-// registers) plus 2 addressable slots held in per-thread shared-memory storage.  Every
-// instruction reads ACC and at most one slot, so no register is ever indexed at run time.
-// Values of ROW kind (one per tile row: row sums, means, rstd) do not live in
-// registers: they live in three shared-memory row buffers (ACC, slot 1, slot 2) and
-// are computed once per row by one thread, then read by the element-wise ops.
+// Registers follow an accumulator machine: ACC (32 fp32 values per thread) lives in
+// registers; the two addressable slots live in tensor memory (TMEM), which this kernel
+// uses as an extension of the register file: tcgen05.st / tcgen05.ld move a whole
+// 32-value register of a thread in one instruction, without touching shared memory.
+// An instruction with a slot operand loads it into one temporary register array, so
+// every opcode has exactly one code path and the interpreter stays small enough for
+// the instruction caches.  A ROW value (one number per tile row: a row sum, mean or
+// rstd) is the same in every lane of a warp and lives in a small per-warp area of
+// shared memory; in programs where all of a thread's vectors lie in one tile row it is
+// computed once.  A row reduction costs a warp butterfly, one partial per warp in
+// shared memory and one CTA barrier.
 //
 // Grid-wide sums (if-else-add's predicate) end a section with a bounded grid barrier in
 // a cooperative launch; the branch is then taken on the device (JLE0), no host
@@ -31,19 +37,23 @@
 
 namespace dvm {
 
-constexpr int NW = kVmWarps;          // warps per CTA
-constexpr int NTHREADS = NW * 32;
-constexpr int REG = kVmReg;           // fp32 values per slot per thread
-constexpr int kMaxRows = 64;          // rows per tile (a >= 128 elements, cap 8192)
+constexpr int NW = kVmWarps;            // warps of the CTA
+constexpr int NCT = NW * 32;            // threads of the CTA
+constexpr int NTHREADS = NCT;
+constexpr int REG = kVmReg;             // fp32 values per FULL register per thread
+constexpr int kMaxRows = 64;            // rows per tile (a >= 128 elements, cap 8192)
+constexpr int kMaxSegs = 64;            // 512-byte segments per tile (8192 fp32 / 128)
+constexpr int kConsumerBar = 1;         // named barrier of the consumer warps
 // shared memory layout
-constexpr int kBarOff = kMaxImage;                    // 17 mbarriers (8 full, 8 empty, 1 hoist)
-constexpr int kRedOff = kBarOff + 256;                // per (row, warp) partial sums
-constexpr int kRowBufOff = kRedOff + kMaxRows * NW * 4;  // 3 row buffers: ACC, slot 1, slot 2
-constexpr int kRowCoordOff = kRowBufOff + 3 * kMaxRows * 4;  // outer coordinates of each tile row
-constexpr int kIssOff = kRowCoordOff + kMaxRows * 4 * 4;  // producer state
-constexpr int kMiscOff = kIssOff + 256;
-constexpr int kSlotOff = kMiscOff + 128;              // slots 1, 2 and a scratch slot 3 (per thread)
-constexpr int kDataOff = kSlotOff + 3 * REG * 4 * NTHREADS;  // hoist area, then the stage ring
+constexpr int kBarOff = kMaxImage;                        // 17 mbarriers (8 full, 8 empty, 1 hoist)
+constexpr int kRedOff = kBarOff + 256;                    // 2 x kMaxSegs row-reduction partials
+constexpr int kRowCoordOff = kRedOff + 2 * kMaxSegs * 4;  // outer coordinates of each tile row
+constexpr int kSegOff = kRowCoordOff + kMaxRows * 16;     // per segment: tile row << 16 | first column
+constexpr int kMiscOff = kSegOff + kMaxSegs * 4;          // grid-sum result, abort flag, CTA partials
+constexpr int kIssOff = kMiscOff + 128;                   // producer state (thread 0)
+constexpr int kRowSlotOff = kIssOff + 384;                // ROW values of ACC, slots 1, 2: [slot][warp][8]
+constexpr int kTmemOff = kRowSlotOff + 3 * NW * 8 * 4;    // TMEM base address
+constexpr int kDataOff = kTmemOff + 128;                  // hoist area, then the stage ring
 static_assert(kDataOff % 128 == 0, "data area alignment");
 static_assert(kDataOff + kSmemBudget <= 227 * 1024, "shared memory of the VEC interpreter");
 
@@ -68,6 +78,8 @@ struct Prog {
   const Instr* body;   // TILES at body[0] for plain programs
   int r, t_in, m, segs, rows;
   int n0, t0, n_in, tiles_in;  // rank <= 2 fast path: outer extent/tile, inner extent, inner tiles
+  int nvu;                     // segments per warp (vectors in use per thread)
+  bool ur;                     // every thread's vectors lie in one tile row
 };
 
 __device__ __forceinline__ void load_prog(const uint8_t* img, int p, Prog& P, int a) {
@@ -84,11 +96,12 @@ __device__ __forceinline__ void load_prog(const uint8_t* img, int p, Prog& P, in
   P.tiles_in = (P.n_in + P.t_in - 1) / P.t_in;
   P.n0 = P.r >= 2 ? (int)P.pr->n[0] : 1;
   P.t0 = P.r >= 2 ? (int)P.pr->t[0] : 1;
+  P.nvu = (P.segs + NW - 1) / NW;
+  P.ur = P.rows == 1 || (P.m >= P.nvu && P.m % P.nvu == 0);
 }
 
 // Position of a tile: local index tau, its tile coordinates and origin.  Rank <= 2
-// tiles are walked incrementally (no division per tile).  Origins are named scalars or
-// arrays indexed only by compile-time constants, so nothing lands in local memory.
+// tiles are walked incrementally (no division per tile).
 struct TilePos {
   int tau;
   int c0, cin;   // tile coordinates (rank <= 2)
@@ -130,7 +143,7 @@ __device__ __forceinline__ void pos_next(const Prog& P, TilePos& T) {
 }
 
 // outer coordinates (within the tile) of tile row `row`, for rank > 2 programs; filled
-// by fill_rowcoords whenever the CTA switches program
+// by fill_tables whenever the CTA switches program
 __device__ __forceinline__ const int* rowcoord(int row) {
   return reinterpret_cast<const int*>(dvm_smem + kRowCoordOff) + (row & (kMaxRows - 1)) * 4;
 }
@@ -160,10 +173,9 @@ __device__ __forceinline__ bool row_off(const Prog& P, const TilePos& O, int row
   return ok;
 }
 
-// the same with divisions and no table, for a tile origin given as scalars (used by the
-// producer thread, which may run ahead into another program, and by the hoist pass)
+// the same with divisions and no table (used by the producer and the hoist pass)
 static __device__ __noinline__ bool row_off_div(const ProgRec* pr, int rank, int od0, int od1, int od2, int row,
-                                         const int64_t* vs, int64_t* off) {
+                                                const int64_t* vs, int64_t* off) {
   int64_t o = 0;
   bool ok = true;
   int rr = row;
@@ -177,11 +189,6 @@ static __device__ __noinline__ bool row_off_div(const ProgRec* pr, int rank, int
   *off = o;
   return ok;
 }
-__device__ __forceinline__ bool row_off_any(const Prog& P, const TilePos& O, int row, const int64_t* vs,
-                                            int64_t& off) {
-  if (P.r <= 2) return row_off(P, O, row, vs, off);
-  return row_off_div(P.pr, P.r, O.od[0], O.od[1], O.od[2], row, vs, &off);
-}
 
 // does a section body contain a stage (DMA, non-hoisted) load?
 __device__ __forceinline__ bool section_has_stage(const Instr* b, int n) {
@@ -190,45 +197,50 @@ __device__ __forceinline__ bool section_has_stage(const Instr* b, int n) {
   return false;
 }
 
+// ---- shared-memory control state ------------------------------------------------
+struct Ctl {
+  int n_stages;
+  uint32_t stage_bytes;
+  uint32_t ring_off;   // byte offset of the stage ring in dvm_smem
+  DevStatus st;
+};
+__device__ __forceinline__ uint64_t* bar_full(int s) { return reinterpret_cast<uint64_t*>(dvm_smem + kBarOff) + s; }
+__device__ __forceinline__ uint64_t* bar_empty(int s) { return reinterpret_cast<uint64_t*>(dvm_smem + kBarOff) + 8 + s; }
+__device__ __forceinline__ uint64_t* bar_hoist() { return reinterpret_cast<uint64_t*>(dvm_smem + kBarOff) + 16; }
+__device__ __forceinline__ float* red_buf(int b) { return reinterpret_cast<float*>(dvm_smem + kRedOff) + b * kMaxSegs; }
+__device__ __forceinline__ float* misc_scalar() { return reinterpret_cast<float*>(dvm_smem + kMiscOff); }
+__device__ __forceinline__ volatile int* abort_flag() { return reinterpret_cast<volatile int*>(dvm_smem + kMiscOff + 16); }
+__device__ __forceinline__ float* cta_partials() { return reinterpret_cast<float*>(dvm_smem + kMiscOff + 64); }
+__device__ __forceinline__ uint8_t* hoist_area() { return dvm_smem + kDataOff; }
+__device__ __forceinline__ void consumer_sync() { named_bar(kConsumerBar, NCT); }
+// ROW values are the same in every lane of a warp (the lanes share their segments), so
+// the ROW parts of ACC and the slots live in a small per-warp area of shared memory
+__device__ __forceinline__ float* rowslot(int k, int warp) {
+  return reinterpret_cast<float*>(dvm_smem + kRowSlotOff) + (k * NW + warp) * 8;
+}
+
 // =========================================================== DMA flow ==
-// Bulk copies of the DMA loads of one tile (or, with hoist_pass, of the hoisted
-// loads at origin 0).  mode 0 counts bytes, mode 1 issues; the caller arms the
-// mbarrier with the count in between.
-__device__ __forceinline__ uint32_t dma_tile(const LaunchParams& Pm, const Prog& P, const Instr* body, int n,
-                                             const TilePos& O, uint8_t* dst_base, uint64_t* bar, bool hoist_pass,
-                                             int mode) {
-  const int r = P.r;
-  const int o_in = O.oin;
-  const int valid_in = min(P.t_in, P.n_in - o_in);
+// Bulk copies of the hoisted (tile-invariant) loads of one program, at origin 0.
+// mode 0 counts bytes, mode 1 issues; the caller arms the mbarrier in between.
+__device__ __forceinline__ uint32_t dma_hoist(const LaunchParams& Pm, const Prog& P, uint8_t* dst_base, uint64_t* bar,
+                                              int mode) {
+  const int valid_in = min(P.t_in, P.n_in);
   uint32_t total = 0;
+  const int n = (int)P.pr->body_len;
   for (int i = 0; i < n; i++) {
-    const Instr w = body[i];
-    if (w.op != OP_LD || (w.flags & (LF_DMA | LF_FIRST)) != (LF_DMA | LF_FIRST)) continue;
-    if (((w.flags & LF_HOIST) != 0) != hoist_pass) continue;
+    const Instr w = P.body[i];
+    if (w.op != OP_LD || (w.flags & (LF_DMA | LF_FIRST | LF_HOIST)) != (LF_DMA | LF_FIRST | LF_HOIST)) continue;
     const TensRec& T = P.tens[w.b];
     const int esz = dtype_size(T.dtype);
     const uint8_t* src = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
     uint8_t* dst = dst_base + w.aux0;
-    if (w.flags & LF_COLV) {
-      int64_t off;
-      if (row_off_any(P, O, 0, T.vs, off)) {
-        total += (uint32_t)(valid_in * esz);
-        if (mode) bulk_g2s(dst, src + (off + o_in) * esz, (uint32_t)(valid_in * esz), bar);
-      }
-    } else if (r == 2 && valid_in == P.t_in && T.vs[0] == (int64_t)P.t_in) {
-      // whole rows of a row-major tensor: the tile is one contiguous block
-      const int nrows = min(P.rows, P.n0 - O.od[0]);
-      const uint32_t bytes = (uint32_t)nrows * P.t_in * esz;
+    const uint32_t bytes = (uint32_t)(valid_in * esz);
+    const int nrows = (w.flags & LF_COLV) ? 1 : P.rows;
+    for (int row = 0; row < nrows; row++) {
+      int64_t off = 0;
+      if (P.r > 1 && !row_off_div(P.pr, P.r, 0, 0, 0, row, T.vs, &off)) continue;
       total += bytes;
-      if (mode) bulk_g2s(dst, src + ((int64_t)O.od[0] * T.vs[0] + o_in) * esz, bytes, bar);
-    } else {
-      const uint32_t bytes = (uint32_t)(valid_in * esz);
-      for (int row = 0; row < P.rows; row++) {
-        int64_t off;
-        if (!row_off_any(P, O, row, T.vs, off)) continue;
-        total += bytes;
-        if (mode) bulk_g2s(dst + (size_t)row * P.t_in * esz, src + (off + o_in) * esz, bytes, bar);
-      }
+      if (mode) bulk_g2s(dst + (size_t)row * P.t_in * esz, src + off * esz, bytes, bar);
     }
   }
   return total;
@@ -251,22 +263,26 @@ struct Issuer {
   int g_end;
   int tau, t_end;  // current program-local range
   int c0, cin;
-  int sec_off, sec_n;  // section body (instruction index, count)
   int stage_sec;   // the section has stage loads
   int issued;      // staged tiles issued so far
-  int n_dma;
-  DmaEnt dma[8];
+  int n;           // stage loads of the section
+  // geometry of the program (copied from its record when the section is set up)
+  int r, t_in, n_in, rows, n0, t0, tiles_in;
+  const ProgRec* pr;
+  const TensRec* tens;
+  DmaEnt e[8];
 };
+static_assert(sizeof(Issuer) <= 384, "issuer state");
+__device__ __forceinline__ Issuer& issuer() { return *reinterpret_cast<Issuer*>(dvm_smem + kIssOff); }
 
 // describe the section's stage (DMA, FIRST, non-hoisted) loads
-__device__ __forceinline__ void issuer_section(Issuer& I, const Prog& P, const LaunchParams& Pm, const Instr* sec,
-                                               int n) {
-  I.n_dma = 0;
-  for (int i = 0; i < n && I.n_dma < 8; i++) {
+__device__ __forceinline__ void dma_section(Issuer& D, const Prog& P, const LaunchParams& Pm, const Instr* sec, int n) {
+  D.n = 0;
+  for (int i = 0; i < n && D.n < 8; i++) {
     const Instr w = sec[i];
     if (w.op != OP_LD || (w.flags & (LF_DMA | LF_FIRST | LF_HOIST)) != (LF_DMA | LF_FIRST)) continue;
     const TensRec& T = P.tens[w.b];
-    DmaEnt& e = I.dma[I.n_dma++];
+    DmaEnt& e = D.e[D.n++];
     e.src = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
     e.vs0 = P.r == 2 ? T.vs[0] : 0;
     e.aux0 = w.aux0;
@@ -277,46 +293,55 @@ __device__ __forceinline__ void issuer_section(Issuer& I, const Prog& P, const L
     else if (P.r <= 2) e.kind = 2;
     else e.kind = 3;
   }
-  I.stage_sec = I.n_dma > 0;
+  D.stage_sec = D.n > 0;
+  D.r = P.r;
+  D.t_in = P.t_in;
+  D.n_in = P.n_in;
+  D.rows = P.rows;
+  D.n0 = P.n0;
+  D.t0 = P.t0;
+  D.tiles_in = P.tiles_in;
+  D.pr = P.pr;
+  D.tens = P.tens;
 }
 
-// one staged tile: arm the full barrier with the byte count, then issue the copies
-__device__ __forceinline__ void issue_tile(const LaunchParams& Pm, const Prog& P, const Issuer& I, const TilePos& O,
-                                           uint8_t* dst_base, uint64_t* bar) {
-  const int o_in = O.oin;
-  const int valid_in = min(P.t_in, P.n_in - o_in);
-  const int nrows = P.r == 2 ? min(P.rows, P.n0 - O.od[0]) : 1;
+// one staged tile at origin (od0..od2, oin): arm the full barrier with the byte count,
+// then issue the copies
+__device__ __forceinline__ void issue_tile(const Issuer& D, int od0, int od1, int od2, int o_in, uint8_t* dst_base,
+                                           uint64_t* bar) {
+  const int valid_in = min(D.t_in, D.n_in - o_in);
+  const int nrows = D.r == 2 ? min(D.rows, D.n0 - od0) : 1;
   for (int mode = 0; mode < 2; mode++) {
     uint32_t total = 0;
-    for (int k = 0; k < I.n_dma; k++) {
-      const DmaEnt& e = I.dma[k];
+    for (int k = 0; k < D.n; k++) {
+      const DmaEnt& e = D.e[k];
       uint8_t* dst = dst_base + e.aux0;
       const uint32_t rowb = (uint32_t)(valid_in * e.esz);
       if (e.kind == 0) {  // one row shared by the tile (outer strides 0 within the tile)
         int64_t off = 0;
         bool ok = true;
-        if (P.r > 2) ok = row_off_div(P.pr, P.r, O.od[0], O.od[1], O.od[2], 0, P.tens[e.tens].vs, &off);
-        else off = (int64_t)O.od[0] * e.vs0;
+        if (D.r > 2) ok = row_off_div(D.pr, D.r, od0, od1, od2, 0, D.tens[e.tens].vs, &off);
+        else off = (int64_t)od0 * e.vs0;
         if (ok) {
           total += rowb;
           if (mode) bulk_g2s(dst, e.src + (off + o_in) * e.esz, rowb, bar);
         }
-      } else if (e.kind == 1 && valid_in == P.t_in) {  // whole rows: one contiguous block
-        const uint32_t bytes = (uint32_t)nrows * P.t_in * e.esz;
+      } else if (e.kind == 1 && valid_in == D.t_in) {  // whole rows: one contiguous block
+        const uint32_t bytes = (uint32_t)nrows * D.t_in * e.esz;
         total += bytes;
-        if (mode) bulk_g2s(dst, e.src + ((int64_t)O.od[0] * e.vs0 + o_in) * e.esz, bytes, bar);
+        if (mode) bulk_g2s(dst, e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz, bytes, bar);
       } else if (e.kind <= 2) {  // rank <= 2, row by row
-        const uint8_t* src = e.src + ((int64_t)O.od[0] * e.vs0 + o_in) * e.esz;
+        const uint8_t* src = e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz;
         total += rowb * nrows;
         if (mode)
           for (int row = 0; row < nrows; row++)
-            bulk_g2s(dst + (size_t)row * P.t_in * e.esz, src + (int64_t)row * e.vs0 * e.esz, rowb, bar);
+            bulk_g2s(dst + (size_t)row * D.t_in * e.esz, src + (int64_t)row * e.vs0 * e.esz, rowb, bar);
       } else {  // rank > 2
-        for (int row = 0; row < P.rows; row++) {
+        for (int row = 0; row < D.rows; row++) {
           int64_t off;
-          if (!row_off_div(P.pr, P.r, O.od[0], O.od[1], O.od[2], row, P.tens[e.tens].vs, &off)) continue;
+          if (!row_off_div(D.pr, D.r, od0, od1, od2, row, D.tens[e.tens].vs, &off)) continue;
           total += rowb;
-          if (mode) bulk_g2s(dst + (size_t)row * P.t_in * e.esz, e.src + (off + o_in) * e.esz, rowb, bar);
+          if (mode) bulk_g2s(dst + (size_t)row * D.t_in * e.esz, e.src + (off + o_in) * e.esz, rowb, bar);
         }
       }
     }
@@ -324,62 +349,58 @@ __device__ __forceinline__ void issue_tile(const LaunchParams& Pm, const Prog& P
   }
 }
 
-// Register slots.  ACC lives in registers (REG values per thread).  The addressable
-// slots 1 and 2, and the scratch slot 3, live in per-thread shared-memory storage laid
-// out [slot][q][thread] in float4 units (conflict-free), which keeps the interpreter
-// loop's register state small enough for large tiles without spills.
-__device__ __forceinline__ float4* slot_ptr(int k, int q) {
-  return reinterpret_cast<float4*>(dvm_smem + kSlotOff) + ((k - 1) * (REG / 4) + q) * NTHREADS + threadIdx.x;
-}
-__device__ __forceinline__ void slot_read(int k, float (&x)[REG]) {
-#pragma unroll
-  for (int q = 0; q < REG / 4; q++) {
-    const float4 f = *slot_ptr(k, q);
-    x[4 * q] = f.x; x[4 * q + 1] = f.y; x[4 * q + 2] = f.z; x[4 * q + 3] = f.w;
-  }
-}
-__device__ __forceinline__ void slot_write(int k, const float (&x)[REG]) {
-#pragma unroll
-  for (int q = 0; q < REG / 4; q++) *slot_ptr(k, q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-}
-
 // ===================================================== consumer helpers ==
 template <int VE>
 struct Lanes {
-  static constexpr int NV = REG / VE;  // vectors (segments) per thread per slot
-  int row[NV];     // tile row of each vector
-  int col[NV];     // first tile column of this lane's VE elements
+  static constexpr int NV = REG / VE;  // vectors per thread per FULL register
+  int s0;          // first segment of this warp
+  int lcol;        // this lane's first column within a segment (lane * VE)
   uint32_t seg;    // bit v: vector v maps to a segment of the tile
   uint32_t rowok;  // bit v: the segment's row lies inside the iteration space (per tile)
+  int rw0, rw1;    // one-row programs: warps whose partials make up this thread's row
+  // tile row and first tile column of vector v (from the program's segment table)
+  __device__ __forceinline__ int row(int v) const { return segtab()[(s0 + v) & (kMaxSegs - 1)] >> 16; }
+  __device__ __forceinline__ int col(int v) const { return (segtab()[(s0 + v) & (kMaxSegs - 1)] & 0xffff) + lcol; }
+  __device__ __forceinline__ static const int* segtab() { return reinterpret_cast<const int*>(dvm_smem + kSegOff); }
 };
 
-// fill the row-coordinate table of a rank > 2 program (all threads call it)
-__device__ __forceinline__ void fill_rowcoords(const Prog& P) {
-  if (P.r <= 2) return;
-  __syncthreads();  // the previous program's tiles may still read the table
-  for (int row = threadIdx.x; row < P.rows; row += NTHREADS) {
-    int* rc = reinterpret_cast<int*>(dvm_smem + kRowCoordOff) + row * 4;
-    int rr = row;
-    for (int d = P.r - 2; d >= 0; d--) {
-      const int td = (int)P.pr->t[d];
-      rc[d] = rr % td;
-      rr /= td;
+// fill the row-coordinate table (rank > 2) and the segment table of a program (all
+// threads call it when the CTA switches program)
+template <int VE>
+__device__ __forceinline__ void fill_tables(const Prog& P) {
+  __syncthreads();  // the previous program's tiles may still read the tables
+  const int a = VE * 32;
+  for (int s = threadIdx.x; s < P.segs; s += NCT)
+    reinterpret_cast<int*>(dvm_smem + kSegOff)[s] = ((s / P.m) << 16) | ((s % P.m) * a);
+  if (P.r > 2) {
+    for (int row = threadIdx.x; row < P.rows; row += NCT) {
+      int* rc = reinterpret_cast<int*>(dvm_smem + kRowCoordOff) + row * 4;
+      int rr = row;
+      for (int d = P.r - 2; d >= 0; d--) {
+        const int td = (int)P.pr->t[d];
+        rc[d] = rr % td;
+        rr /= td;
+      }
     }
   }
   __syncthreads();
 }
 
+// Segments (512-byte runs of one tile row) are dealt to warps in blocks: warp w holds
+// segments [w*nvu, (w+1)*nvu), one per vector of each lane.
 template <int VE>
 __device__ __forceinline__ void lanes_for_prog(const Prog& P, int warp, int lane, Lanes<VE>& L) {
-  const int a = VE * 32;
+  L.s0 = warp * P.nvu;
+  L.lcol = lane * VE;
   L.seg = 0;
 #pragma unroll
-  for (int v = 0; v < Lanes<VE>::NV; v++) {
-    const int s = v * NW + warp;
-    if (s < P.segs) L.seg |= 1u << v;
-    L.row[v] = s / P.m;
-    L.col[v] = (s % P.m) * a + lane * VE;
-  }
+  for (int v = 0; v < Lanes<VE>::NV; v++)
+    if (v < P.nvu && L.s0 + v < P.segs) L.seg |= 1u << v;
+  // one-row programs: the warps holding this thread's row
+  const int r = min(L.s0 / P.m, kMaxRows - 1);
+  const int wl = (P.segs + P.nvu - 1) / P.nvu;
+  L.rw0 = (r * P.m) / P.nvu;
+  L.rw1 = min(((r + 1) * P.m + P.nvu - 1) / P.nvu, wl);
 }
 
 template <int VE>
@@ -387,11 +408,13 @@ __device__ __forceinline__ void lanes_for_tile(const Prog& P, const TilePos& O, 
   uint32_t ok = 0;
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
-    bool in = (L.seg >> v) & 1u;
+    if (!((L.seg >> v) & 1u)) continue;
+    const int row = L.row(v);
+    bool in = true;
     if (P.r == 2) {
-      in = in && (O.od[0] + L.row[v] < P.n0);
+      in = O.od[0] + row < P.n0;
     } else if (P.r > 2) {
-      const int* rc = rowcoord(L.row[v]);
+      const int* rc = rowcoord(row);
 #pragma unroll
       for (int dd = 0; dd < 3; dd++)
         if (dd < P.r - 1) in = in && (O.od[dd] + rc[dd] < (int)P.pr->n[dd]);
@@ -404,11 +427,96 @@ __device__ __forceinline__ void lanes_for_tile(const Prog& P, const TilePos& O, 
 // valid elements of vector v among its VE (the inner tail of the last column tile)
 template <int VE>
 __device__ __forceinline__ int ncol(const Prog& P, const TilePos& O, const Lanes<VE>& L, int v) {
-  const int nc = P.n_in - (O.oin + L.col[v]);
+  const int nc = P.n_in - (O.oin + L.col(v));
   return nc < 0 ? 0 : (nc > VE ? VE : nc);
 }
 
-// ---- loads into a register slot -------------------------------------------
+// ---- tensor memory -------------------------------------------------------------
+// Each CTA allocates all 512 TMEM columns.  Warp w may access lanes 32*(w%4)..+31; the
+// warps w and w+4 share those lanes and split the columns.  Per thread: slot 1 at
+// columns [0, 32), slot 2 at [32, 64), the scratch register at [64, 96) and a spare
+// register at [96, 128) of its half.
+constexpr uint32_t kTmemCols = 512;
+__device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t tm_base(uint32_t tmem) {
+  const int warp = threadIdx.x >> 5;
+  return tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 256);
+}
+__device__ __forceinline__ uint32_t tm_slot(uint32_t tb, int k) { return tb + (uint32_t)(k - 1) * 32u; }
+__device__ __forceinline__ uint32_t tm_scratch(uint32_t tb) { return tb + 64u; }
+
+// 32 columns of this thread's lane <-> 32 registers; each access waits for its own
+// completion (the wait is in the same statement, so no use of the registers can be
+// scheduled before the data is there, and no later access can overtake a store)
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[REG]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[REG]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+      "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+      "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ float4 tm_ld4(uint32_t taddr) {
+  uint32_t a, b, c, d;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\ttcgen05.wait::ld.sync.aligned;"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(taddr)
+               : "memory");
+  return make_float4(__uint_as_float(a), __uint_as_float(b), __uint_as_float(c), __uint_as_float(d));
+}
+__device__ __forceinline__ void tm_st4(uint32_t taddr, float4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+               "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w))
+               : "memory");
+}
+__device__ __forceinline__ float tm_ld1(uint32_t taddr) {
+  uint32_t a;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
+               : "=r"(a)
+               : "r"(taddr)
+               : "memory");
+  return __uint_as_float(a);
+}
+__device__ __forceinline__ void tm_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+               "r"(__float_as_uint(v))
+               : "memory");
+}
+
+// ---- loads into a FULL register ------------------------------------------
 template <int VE, int ESZ>
 __device__ __forceinline__ void unpack(const uint8_t* p, float* dst) {
   if constexpr (ESZ == 4) {
@@ -440,43 +548,36 @@ __device__ __forceinline__ float load_scalar(const uint8_t* base, int64_t off, i
   return (float)__ldg(base + off);
 }
 
-// Hot paths are straight-line: the element size is resolved once per instruction, and
-// per-vector validity turns into address clamping (shared memory) or a warp-uniform
-// choice between a full-tile loop and a general masked loop (global memory).
 template <int VE, int ESZ>
 __device__ __forceinline__ void lds_vectors(float (&dst)[REG], const uint8_t* region, int rstride,
                                             const Lanes<VE>& L) {
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
-    const bool in = (L.seg >> v) & 1u;
-    const int eo = in ? (L.row[v] * rstride + L.col[v]) : 0;  // clamp: row 0, column 0 is inside
-    unpack<VE, ESZ>(region + (size_t)eo * ESZ, dst + v * VE);
+    if (!((L.seg >> v) & 1u)) continue;   // warp-uniform
+    unpack<VE, ESZ>(region + (size_t)(L.row(v) * rstride + L.col(v)) * ESZ, dst + v * VE);
   }
 }
 
 template <int VE, int ESZ>
 __device__ __forceinline__ void ldg_vectors_fast(float (&dst)[REG], const uint8_t* base, int64_t vs0, int oin,
                                                  const TilePos& O, const Lanes<VE>& L) {
-  // rank <= 2, inner stride 1, every vector of the thread inside the tensor
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
     if (!((L.seg >> v) & 1u)) continue;
-    const int64_t off = (int64_t)(O.od[0] + L.row[v]) * vs0 + oin + L.col[v];
+    const int64_t off = (int64_t)(O.od[0] + L.row(v)) * vs0 + oin + L.col(v);
     unpack<VE, ESZ>(base + off * ESZ, dst + v * VE);
   }
 }
 
-// LD of a FULL value into registers
-// `scratch` is a slot whose contents are dead (used by the masked path)
+// LD of a FULL value
 template <int VE>
 __device__ __forceinline__ void op_load(float (&dst)[REG], const Instr& w, const Prog& P, const Lanes<VE>& L,
                                         const TilePos& O, const LaunchParams& Pm, const uint8_t* stage_base,
-                                        const uint8_t* hoist_base, int scratch) {
-  constexpr int NV = Lanes<VE>::NV;
+                                        uint32_t tb) {
   const TensRec& T = P.tens[w.b];
   const int dt = T.dtype;
   if (w.flags & LF_DMA) {
-    const uint8_t* region = ((w.flags & LF_HOIST) ? hoist_base + P.pr->hoist_base : stage_base) + w.aux0;
+    const uint8_t* region = ((w.flags & LF_HOIST) ? hoist_area() + P.pr->hoist_base : stage_base) + w.aux0;
     const int rstride = (w.flags & LF_COLV) ? 0 : P.t_in;
     if (dt == DT_F32) {
       lds_vectors<VE, 4>(dst, region, rstride, L);
@@ -505,21 +606,21 @@ __device__ __forceinline__ void op_load(float (&dst)[REG], const Instr& w, const
     return;
   }
   // general masked path (ragged tails, strided views, rank > 2): a rolled loop through
-  // the scratch slot keeps it compact
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sc = reinterpret_cast<float*>(dvm_smem + kSlotOff) + (scratch - 1) * REG * NTHREADS;  // [q][thread][4]
+  // the TMEM scratch register keeps it compact
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
 #pragma unroll 1
   for (int j = 0; j < REG; j++) {
     const int v = j / VE, e = j % VE;
-    const int sgi = v * NW + warp;
-    const int row = sgi / P.m, col = (sgi % P.m) * (VE * 32) + lane * VE;
+    const int s = warp * P.nvu + v;
+    const int row = s / P.m, col = (s % P.m) * (VE * 32) + lane * VE;
     float x = 0.f;
     int64_t off;
-    if (sgi < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
+    if (v < P.nvu && s < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
       x = load_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt);
-    sc[((j >> 2) * NTHREADS + threadIdx.x) * 4 + (j & 3)] = x;
+    tm_st1(tm_scratch(tb) + (uint32_t)j, x);
   }
-  slot_read(scratch, dst);
+  tm_ld32(tm_scratch(tb), dst);
 }
 
 // ---- stores from ACC --------------------------------------------------------
@@ -559,15 +660,14 @@ __device__ __forceinline__ void stg_vectors_fast(const float (&acc)[REG], uint8_
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
     if (!((L.seg >> v) & 1u)) continue;
-    const int64_t off = (int64_t)(O.od[0] + L.row[v]) * vs0 + oin + L.col[v];
+    const int64_t off = (int64_t)(O.od[0] + L.row(v)) * vs0 + oin + L.col(v);
     pack_store<VE, ESZ>(base + off * ESZ, acc + v * VE);
   }
 }
 
 template <int VE>
 __device__ __forceinline__ void op_store(const float (&acc)[REG], const Instr& w, const Prog& P, const Lanes<VE>& L,
-                                         const TilePos& O, const LaunchParams& Pm) {
-  constexpr int NV = Lanes<VE>::NV;
+                                         const TilePos& O, const LaunchParams& Pm, uint32_t tb) {
   const TensRec& T = P.tens[w.a];
   const int dt = T.dtype;
   const int esz = dtype_size(dt);
@@ -586,17 +686,18 @@ __device__ __forceinline__ void op_store(const float (&acc)[REG], const Instr& w
     }
     return;
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  slot_write(3, acc);
-  const float* sc = reinterpret_cast<const float*>(dvm_smem + kSlotOff) + 2 * REG * NTHREADS;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  tm_st32(tm_scratch(tb), acc);
 #pragma unroll 1
   for (int j = 0; j < REG; j++) {
     const int v = j / VE, e = j % VE;
-    const int sgi = v * NW + warp;
-    const int row = sgi / P.m, col = (sgi % P.m) * (VE * 32) + lane * VE;
+    const int s = warp * P.nvu + v;
+    const int row = s / P.m, col = (s % P.m) * (VE * 32) + lane * VE;
+    const float x = tm_ld1(tm_scratch(tb) + (uint32_t)j);
     int64_t off;
-    if (sgi < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
-      store_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt, sc[((j >> 2) * NTHREADS + threadIdx.x) * 4 + (j & 3)]);
+    if (v < P.nvu && s < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
+      store_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt, x);
   }
 }
 
@@ -628,17 +729,7 @@ __device__ __forceinline__ float pow_fast(float a, float b) {
   return powf(a, b);
 }
 
-template <int OP>
-__device__ __forceinline__ float bin(float a, float b) {
-  if constexpr (OP == OP_ADD) return a + b;
-  else if constexpr (OP == OP_SUB) return a - b;
-  else if constexpr (OP == OP_MUL) return a * b;
-  else if constexpr (OP == OP_DIV) return a / b;
-  else if constexpr (OP == OP_MAX) return vmax(a, b);
-  else if constexpr (OP == OP_MIN) return vmin(a, b);
-  else return powf(a, b);
-}
-__device__ __forceinline__ float bin_rt(int op, float a, float b) {  // runtime opcode (row values)
+__device__ __forceinline__ float bin_rt(int op, float a, float b) {  // runtime opcode (scalars)
   switch (op) {
     case OP_ADD: return a + b;
     case OP_SUB: return a - b;
@@ -650,62 +741,83 @@ __device__ __forceinline__ float bin_rt(int op, float a, float b) {  // runtime 
   }
 }
 
-// ACC (FULL) <- op(ACC, X) where X is a FULL value, a ROW buffer, or an immediate.
-// The operand order is resolved outside the unrolled loops.
+// Packed fp32 pairs: one instruction gives two IEEE round-to-nearest results.
+template <int OP>
+__device__ __forceinline__ void pair_op(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  if constexpr (OP == OP_ADD) {
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  } else if constexpr (OP == OP_SUB) {
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  } else if constexpr (OP == OP_MUL) {
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  } else if constexpr (OP == OP_MAX) {
+    d0 = vmax(a0, b0);
+    d1 = vmax(a1, b1);
+  } else {
+    d0 = vmin(a0, b0);
+    d1 = vmin(a1, b1);
+  }
+}
+
 template <int OP>
 __host__ __device__ constexpr bool commutative() { return OP == OP_ADD || OP == OP_MUL || OP == OP_MAX || OP == OP_MIN; }
 
+// ACC <- ACC op X (REV: X op ACC), X a FULL register
 template <int OP, bool REV>
 __device__ __forceinline__ void bin_ff_(float (&acc)[REG], const float (&x)[REG]) {
 #pragma unroll
-  for (int e = 0; e < REG; e++) acc[e] = REV ? bin<OP>(x[e], acc[e]) : bin<OP>(acc[e], x[e]);
+  for (int e = 0; e < REG; e += 2) {
+    if (REV) pair_op<OP>(acc[e], acc[e + 1], x[e], x[e + 1], acc[e], acc[e + 1]);
+    else pair_op<OP>(acc[e], acc[e + 1], acc[e], acc[e + 1], x[e], x[e + 1]);
+  }
 }
 template <int OP>
 __device__ __forceinline__ void bin_ff(float (&acc)[REG], const float (&x)[REG], bool rev) {
   if (!commutative<OP>() && rev) bin_ff_<OP, true>(acc, x);
   else bin_ff_<OP, false>(acc, x);
 }
-template <int OP, bool REV>
-__device__ __forceinline__ void bin_fi_(float (&acc)[REG], float x) {
-#pragma unroll
-  for (int e = 0; e < REG; e++) acc[e] = REV ? bin<OP>(x, acc[e]) : bin<OP>(acc[e], x);
-}
-template <int OP>
-__device__ __forceinline__ void bin_fi(float (&acc)[REG], float x, bool rev) {
-  if (!commutative<OP>() && rev) bin_fi_<OP, true>(acc, x);
-  else bin_fi_<OP, false>(acc, x);
-}
-// FULL op ROW(row buffer xrow) -> FULL
+// ACC <- ACC op x (one value per vector: an immediate or a ROW register)
 template <int VE, int OP, bool REV>
-__device__ __forceinline__ void bin_fr_(float (&acc)[REG], const float* xrow, const Lanes<VE>& L) {
+__device__ __forceinline__ void bin_fv_(float (&acc)[REG], const float (&xv)[REG / VE]) {
 #pragma unroll
-  for (int v = 0; v < Lanes<VE>::NV; v++) {
-    const float x0 = xrow[L.row[v] & (kMaxRows - 1)];
+  for (int v = 0; v < REG / VE; v++) {
+    const float x0 = xv[v];
 #pragma unroll
-    for (int e = 0; e < VE; e++) acc[v * VE + e] = REV ? bin<OP>(x0, acc[v * VE + e]) : bin<OP>(acc[v * VE + e], x0);
+    for (int e = v * VE; e < v * VE + VE; e += 2) {
+      if (REV) pair_op<OP>(acc[e], acc[e + 1], x0, x0, acc[e], acc[e + 1]);
+      else pair_op<OP>(acc[e], acc[e + 1], acc[e], acc[e + 1], x0, x0);
+    }
   }
 }
 template <int VE, int OP>
-__device__ __forceinline__ void bin_fr(float (&acc)[REG], const float* xrow, const Lanes<VE>& L, bool rev) {
-  if (!commutative<OP>() && rev) bin_fr_<VE, OP, true>(acc, xrow, L);
-  else bin_fr_<VE, OP, false>(acc, xrow, L);
+__device__ __forceinline__ void bin_fv(float (&acc)[REG], const float (&xv)[REG / VE], bool rev) {
+  if (!commutative<OP>() && rev) bin_fv_<VE, OP, true>(acc, xv);
+  else bin_fv_<VE, OP, false>(acc, xv);
 }
-// ROW(row buffer arow) op FULL x -> FULL in ACC
+// ACC <- a op X (REV: X op a), `a` one value per vector (ACC holds a ROW value)
 template <int VE, int OP, bool REV>
-__device__ __forceinline__ void bin_rf_(float (&acc)[REG], const float* arow, const float (&x)[REG],
-                                        const Lanes<VE>& L) {
+__device__ __forceinline__ void bin_vf_(float (&acc)[REG], const float (&av)[REG / VE], const float (&x)[REG]) {
 #pragma unroll
-  for (int v = 0; v < Lanes<VE>::NV; v++) {
-    const float a0 = arow[L.row[v] & (kMaxRows - 1)];
+  for (int v = 0; v < REG / VE; v++) {
+    const float a0 = av[v];
 #pragma unroll
-    for (int e = 0; e < VE; e++) acc[v * VE + e] = REV ? bin<OP>(x[v * VE + e], a0) : bin<OP>(a0, x[v * VE + e]);
+    for (int e = v * VE; e < v * VE + VE; e += 2) {
+      if (REV) pair_op<OP>(acc[e], acc[e + 1], x[e], x[e + 1], a0, a0);
+      else pair_op<OP>(acc[e], acc[e + 1], a0, a0, x[e], x[e + 1]);
+    }
   }
 }
 template <int VE, int OP>
-__device__ __forceinline__ void bin_rf(float (&acc)[REG], const float* arow, const float (&x)[REG], const Lanes<VE>& L,
+__device__ __forceinline__ void bin_vf(float (&acc)[REG], const float (&av)[REG / VE], const float (&x)[REG],
                                        bool rev) {
-  if (!commutative<OP>() && rev) bin_rf_<VE, OP, true>(acc, arow, x, L);
-  else bin_rf_<VE, OP, false>(acc, arow, x, L);
+  if (!commutative<OP>() && rev) bin_vf_<VE, OP, true>(acc, av, x);
+  else bin_vf_<VE, OP, false>(acc, av, x);
 }
 
 // warp-level all-reduce (xor butterfly: every lane ends with identical bits)
@@ -719,203 +831,98 @@ __device__ __forceinline__ float warp_reduce(float p) {
   return p;
 }
 
-// ---- the CTA's work ---------------------------------------------------------
-// Shared-memory control state is addressed from dvm_smem with constant offsets so that
-// no generic pointers occupy registers; only the ring geometry is kept in registers.
-struct Ctl {
-  int n_stages;
-  uint32_t stage_bytes;
-  uint32_t ring_off;   // byte offset of the stage ring in dvm_smem
-  DevStatus st;
-};
-__device__ __forceinline__ uint64_t* bar_full(int s) { return reinterpret_cast<uint64_t*>(dvm_smem + kBarOff) + s; }
-__device__ __forceinline__ uint64_t* bar_empty(int s) { return reinterpret_cast<uint64_t*>(dvm_smem + kBarOff) + 8 + s; }
-__device__ __forceinline__ uint64_t* bar_hoist() { return reinterpret_cast<uint64_t*>(dvm_smem + kBarOff) + 16; }
-__device__ __forceinline__ float* red_buf() { return reinterpret_cast<float*>(dvm_smem + kRedOff); }
-__device__ __forceinline__ float* row_buf() { return reinterpret_cast<float*>(dvm_smem + kRowBufOff); }
-__device__ __forceinline__ Issuer& issuer() { return *reinterpret_cast<Issuer*>(dvm_smem + kIssOff); }
-__device__ __forceinline__ float* misc_scalar() { return reinterpret_cast<float*>(dvm_smem + kMiscOff); }
-__device__ __forceinline__ volatile int* abort_flag() { return reinterpret_cast<volatile int*>(dvm_smem + kMiscOff + 16); }
-__device__ __forceinline__ uint8_t* hoist_area() { return dvm_smem + kDataOff; }
-
 // ---- heavy math -------------------------------------------------------------
 // Transcendental and correctly rounded ops (sqrt, rsqrt, recip, log, exp, silu, div,
-// pow) are long instruction sequences; unrolling them over the 16 register values in
-// every operand form would make the interpreter's code far larger than the instruction
-// caches.  They run instead as a rolled loop, 4 values per iteration, over the thread's
-// scratch slot (slot 3) in shared memory: ACC is written there, transformed, and read
-// back.  Light ops (add, sub, mul, max, min, abs, neg, floor, round, casts) stay
-// unrolled in registers.
+// pow) are long instruction sequences.  They run as a rolled loop, 4 values per
+// iteration, over the thread's scratch register in TMEM, so each appears once in the
+// interpreter's code.
 __device__ __forceinline__ bool heavy_unary(int op) {
   return op == OP_SQRT || op == OP_LOG || op == OP_EXP || op == OP_RSQRT || op == OP_RECIP || op == OP_SILU;
 }
-
-template <class F>
-__device__ __forceinline__ float4 map4(float4 a, F f) {
-  a.x = f(a.x); a.y = f(a.y); a.z = f(a.z); a.w = f(a.w);
-  return a;
-}
-
-__device__ __forceinline__ void heavy_unary_loop(int op) {
-  switch (op) {
-#define DVM_HEAVY_U(OPC, EXPR)                                         \
-  case OPC:                                                            \
-    _Pragma("unroll 1") for (int q = 0; q < REG / 4; q++) {            \
-      float4* p = slot_ptr(3, q);                                      \
-      *p = map4(*p, [](float x) { return EXPR; });                     \
-    }                                                                  \
-    break;
-    DVM_HEAVY_U(OP_SQRT, sqrtf(x))
-    DVM_HEAVY_U(OP_RSQRT, 1.0f / sqrtf(x))
-    DVM_HEAVY_U(OP_RECIP, 1.0f / x)
-    DVM_HEAVY_U(OP_LOG, logf(x))
-    DVM_HEAVY_U(OP_EXP, expf(x))
-    DVM_HEAVY_U(OP_SILU, x / (1.0f + expf(-x)))
-#undef DVM_HEAVY_U
-    default: break;
-  }
-}
-
 __device__ __forceinline__ float4 splat4(float v) { return make_float4(v, v, v, v); }
 
-// ACC <- op(A, X) for DIV / POW (result FULL).  A is the scratch slot 3 (ACC written
-// there) or, with arow, the ACC row buffer; X is an immediate (xslot < 0), ACC itself
-// (xslot == 0), a slot (1, 2), or, with xrow != nullptr, a row buffer.
-template <int VE>
-__device__ __forceinline__ void heavy_binary_loop(int op, bool rev, bool arow, const float* xrow, int xslot, float xi,
-                                                  int m) {
-  const int warp = threadIdx.x >> 5;
-  const float* RB = row_buf();
+// ACC <- op(ACC) through the scratch register
+__device__ __forceinline__ void heavy_unary_loop(int op, uint32_t sc) {
 #pragma unroll 1
   for (int q = 0; q < REG / 4; q++) {
-    int row = 0;
-    if (arow || xrow) {  // the 4 values of iteration q lie in one segment (VE >= 4)
-      const int v = (4 * q) / VE;
-      row = ((v * NW + warp) / m) & (kMaxRows - 1);
-    }
-    float4* pa = slot_ptr(3, q);
-    const float4 a = arow ? splat4(RB[row]) : *pa;
-    const float4 x = xrow ? splat4(xrow[row]) : xslot > 0 ? *slot_ptr(xslot, q) : xslot == 0 ? a : splat4(xi);
+    float4 x = tm_ld4(sc + 4u * q);
+    x.x = unary_fn(op, x.x);
+    x.y = unary_fn(op, x.y);
+    x.z = unary_fn(op, x.z);
+    x.w = unary_fn(op, x.w);
+    tm_st4(sc + 4u * q, x);
+  }
+}
+// scratch <- scratch op X (REV: X op scratch) for DIV / POW.  X is a register in TMEM
+// at column address xcol (x_tm), one value per vector from a ROW area in shared memory
+// (xrow), or an immediate.  (A TMEM address can be 0: lane 0, column 0.)
+__device__ __forceinline__ void heavy_binary_loop(int op, bool rev, uint32_t sc, bool x_tm, uint32_t xcol,
+                                                  const float* xrow, float xi, int ve) {
+#pragma unroll 1
+  for (int q = 0; q < REG / 4; q++) {
+    const float4 a = tm_ld4(sc + 4u * q);
+    const float4 x = x_tm ? tm_ld4(xcol + 4u * q) : splat4(xrow ? xrow[(4 * q) / ve] : xi);
     const float4 l = rev ? x : a, r = rev ? a : x;
     float4 o;
-    if (op == OP_DIV) {
-      o = make_float4(l.x / r.x, l.y / r.y, l.z / r.z, l.w / r.w);
-    } else {
-      o = make_float4(pow_fast(l.x, r.x), pow_fast(l.y, r.y), pow_fast(l.z, r.z), pow_fast(l.w, r.w));
-    }
-    *pa = o;
+    if (op == OP_DIV) o = make_float4(l.x / r.x, l.y / r.y, l.z / r.z, l.w / r.w);
+    else o = make_float4(pow_fast(l.x, r.x), pow_fast(l.y, r.y), pow_fast(l.z, r.z), pow_fast(l.w, r.w));
+    tm_st4(sc + 4u * q, o);
+  }
+}
+// ROW op: one value (one-row programs) or one per vector, in a per-warp ROW area
+__device__ __forceinline__ void row_binary(int op, bool rev, float* dst, const float* xrow, float xi, int nv) {
+  __syncwarp();
+#pragma unroll 1
+  for (int v = 0; v < nv; v++) {
+    const float a = dst[v], x = xrow ? xrow[v] : xi;
+    const float r = rev ? bin_rt(op, x, a) : bin_rt(op, a, x);
+    __syncwarp();
+    dst[v] = r;
+    __syncwarp();
+  }
+}
+__device__ __forceinline__ void row_unary(int op, float* dst, int nv) {
+  __syncwarp();
+#pragma unroll 1
+  for (int v = 0; v < nv; v++) {
+    const float r = unary_fn(op, dst[v]);
+    __syncwarp();
+    dst[v] = r;
+    __syncwarp();
   }
 }
 
-
-// Thread 0: issue staged tiles of the current range until `limit` tiles are issued.
-__device__ __forceinline__ void issue_upto(const LaunchParams& Pm, const uint8_t* img, const Ctl& C, int a,
-                                           int limit, bool plain) {
-  Issuer& I = issuer();
-  while (I.issued < limit && !*abort_flag()) {
-    if (plain) {
-      while (true) {
-        if (I.g >= I.g_end) return;
-        const ProgRec* pr = reinterpret_cast<const ProgRec*>(img + sizeof(Header) + I.prog * sizeof(ProgRec));
-        const int end = (int)(pr->tile_base + pr->block_dim);
-        if (I.g >= end) {  // the current program is done: set up the next one
-          I.prog++;
-          Prog Q;
-          load_prog(img, I.prog, Q, a);
-          I.sec_off = (int)(Q.pr->body_off / sizeof(Instr)) + 1;
-          I.sec_n = (int)Q.body[0].imm;
-          issuer_section(I, Q, Pm, Q.body + 1, I.sec_n);
-          I.tau = I.g - (int)Q.pr->tile_base;
-          I.c0 = I.tau / Q.tiles_in;
-          I.cin = I.tau - I.c0 * Q.tiles_in;
-          continue;
-        }
-        if (!I.stage_sec) {  // nothing to stage in this program: skip its tiles
-          I.g = end;
-          continue;
-        }
-        break;
-      }
-    } else if (I.tau >= I.t_end || !I.stage_sec) {
-      return;
-    }
-    Prog P;
-    load_prog(img, I.prog, P, a);
-    TilePos T;
-    T.tau = I.tau;
-    T.c0 = I.c0;
-    T.cin = I.cin;
-    pos_origin(P, T);
-    const int stage = I.issued % C.n_stages;
-    const uint32_t parity = ((I.issued / C.n_stages) & 1) ^ 1;
-    if (!mbar_wait(bar_empty(stage), parity, C.st, abort_flag())) return;
-    issue_tile(Pm, P, I, T, dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes, bar_full(stage));
-    I.issued++;
-    I.tau++;
-    if (++I.cin == P.tiles_in) {
-      I.cin = 0;
-      I.c0++;
-    }
-    if (plain) I.g++;
-  }
+// ROW values are the same in every lane of a warp; after a one-row update the first
+// value is copied to the thread's other vectors
+__device__ __forceinline__ void row_fill(float* dst, int nv) {
+  __syncwarp();
+  const float r0 = dst[0];
+  for (int v = 1; v < nv; v++) dst[v] = r0;
+  __syncwarp();
 }
 
-// Element-wise op with opcode OPC on the accumulator, all operand forms.
-#define DVM_BIN_CASE(OPC)                                               \
-  case OPC:                                                             \
-    if (imm) {                                                          \
-      bin_fi<OPC>(R0, __uint_as_float(w.imm), rev);                     \
-    } else if (ar) {                                                    \
-      row_cross_read();                                                 \
-      float X[REG];                                                     \
-      slot_read(w.a, X);                                                \
-      bin_rf<VE, OPC>(R0, RB, X, L, rev);                               \
-    } else if (xr) {                                                    \
-      row_cross_read();                                                 \
-      bin_fr<VE, OPC>(R0, RB + w.a * kMaxRows, L, rev);                 \
-    } else if (w.a == 0) {                                              \
-      bin_ff<OPC>(R0, R0, rev);                                         \
-    } else {                                                            \
-      float X[REG];                                                     \
-      slot_read(w.a, X);                                                \
-      bin_ff<OPC>(R0, X, rev);                                          \
-    }                                                                   \
-    break;
-
-// ROW-buffer loop: entry r belongs to thread r
-#define DVM_ROWS_FOR(r) for (int r = threadIdx.x; r < P.rows; r += NTHREADS)
+template <int VE>
+__device__ __forceinline__ void bcast_row(float (&acc)[REG], const float* qv) {
+#pragma unroll
+  for (int v = 0; v < REG / VE; v++) {
+    const float x0 = qv[v];
+#pragma unroll
+    for (int e = 0; e < VE; e++) acc[v * VE + e] = x0;
+  }
+}
 
 template <int VE>
 __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P, const Instr* body, int n,
-                                          const TilePos& T, Lanes<VE>& L, int lane, int it, const Ctl& C,
-                                          float& grand, float (&R0)[REG], bool& row_read, bool& row_dirty) {
+                                          const TilePos& O, Lanes<VE>& L, int lane, int it, const Ctl& C,
+                                          float& grand, float (&A)[REG], int& rbuf, uint32_t tb) {
   constexpr int NV = REG / VE;
-  const TilePos& O = T;
+  const int warp = threadIdx.x >> 5;
+  float* Q0 = rowslot(0, warp);   // ROW value of ACC (per vector)
+  const int nvr = P.ur ? 1 : NV;  // ROW values that differ within a thread
   lanes_for_tile<VE>(P, O, L);
   const int stage = C.n_stages ? it % C.n_stages : 0;
   const uint32_t parity = C.n_stages ? (uint32_t)((it / C.n_stages) & 1) : 0;
   const uint8_t* stage_base = dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes;
-  const int warp = threadIdx.x >> 5;
-  float* RB = row_buf();  // RB[k * kMaxRows + r]
-  // Row buffers: entry r is written only by its owner thread (threadIdx.x == r) and
-  // read either by the owner or by every thread (element-wise ops with a ROW operand).
-  // A CTA barrier is needed before a cross-thread read that follows owner writes
-  // (row_dirty), and before an owner write that follows cross-thread reads (row_read).
-  auto row_write_begin = [&]() {
-    if (row_read) {
-      __syncthreads();
-      row_read = false;
-      row_dirty = false;
-    }
-  };
-  auto row_write_end = [&]() { row_dirty = true; };
-  auto row_cross_read = [&]() {
-    if (row_dirty) {
-      __syncthreads();
-      row_dirty = false;
-    }
-    row_read = true;
-  };
   for (int pc = 0; pc < n; pc++) {
     const Instr w = body[pc];
     const uint8_t fl = w.flags;
@@ -930,135 +937,218 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
       case OP_LD:
         if (fl & LF_ROWV) {
           // one value per tile row from a [.., 1]-shaped tensor
-          row_write_begin();
           const TensRec& Tn = P.tens[w.b];
           const uint8_t* base = static_cast<const uint8_t*>(Pm.ptrs[Tn.binding]);
-          float* dstrow = RB + w.a * kMaxRows;
-          DVM_ROWS_FOR(r) {
+          float* dst = rowslot(w.a, warp);
+          __syncwarp();
+#pragma unroll 1
+          for (int v = 0; v < nvr; v++) {
+            float q = 0.f;
             int64_t off;
-            dstrow[r] = row_off(P, O, r, Tn.vs, off) ? load_scalar(base, off, Tn.dtype) : 0.f;
+            if (((L.rowok >> v) & 1u) && row_off(P, O, L.row(v), Tn.vs, off)) q = load_scalar(base, off, Tn.dtype);
+            dst[v] = q;
           }
-          row_write_end();
+          if (P.ur) row_fill(dst, NV);
+          __syncwarp();
+        } else if (w.a == 0) {
+          op_load<VE>(A, w, P, L, O, Pm, stage_base, tb);
         } else {
-          // one load path into ACC; a load into a slot parks ACC in the scratch slot
-          if (w.a != 0) slot_write(3, R0);
-          op_load<VE>(R0, w, P, L, O, Pm, stage_base, hoist_area(), w.a != 0 ? (int)w.a : 3);
-          if (w.a != 0) {
-            slot_write(w.a, R0);
-            slot_read(3, R0);
-          }
+          float X[REG];
+          op_load<VE>(X, w, P, L, O, Pm, stage_base, tb);
+          tm_st32(tm_slot(tb, w.a), X);
         }
         break;
       case OP_ST:
         if (fl & LF_ROWV) {
+          // the row's first segment (lane 0) writes it
           const TensRec& Tn = P.tens[w.a];
           uint8_t* base = static_cast<uint8_t*>(Pm.ptrs[Tn.binding]);
-          DVM_ROWS_FOR(r) {
+#pragma unroll 1
+          for (int v = 0; v < NV; v++) {
+            const int s = warp * P.nvu + v;
             int64_t off;
-            if (row_off(P, O, r, Tn.vs, off)) store_scalar(base, off, Tn.dtype, RB[r]);
+            if (lane == 0 && ((L.rowok >> v) & 1u) && s % P.m == 0 && row_off(P, O, L.row(v), Tn.vs, off))
+              store_scalar(base, off, Tn.dtype, Q0[v]);
           }
         } else {
-          op_store<VE>(R0, w, P, L, O, Pm);
+          op_store<VE>(A, w, P, L, O, Pm, tb);
         }
         break;
       case OP_MOV:
-        if (fl & 1) {  // ROW value: copy between row buffers (owner threads)
-          row_write_begin();
-          DVM_ROWS_FOR(r) RB[w.a * kMaxRows + r] = RB[w.b * kMaxRows + r];
-          row_write_end();
+        if (fl & 1) {  // ROW value: copy between per-warp ROW areas
+          const float* src = rowslot(w.b, warp);
+          float* dst = rowslot(w.a, warp);
+          __syncwarp();
+          float t[NV];
+#pragma unroll
+          for (int v = 0; v < NV; v++) t[v] = src[v];
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < NV; v++) dst[v] = t[v];
+          __syncwarp();
         } else if (w.a == 0) {
-          if (w.b != 0) slot_read(w.b, R0);
+          if (w.b != 0) tm_ld32(tm_slot(tb, w.b), A);
+        } else if (w.b == 0) {
+          tm_st32(tm_slot(tb, w.a), A);
         } else {
-          slot_write(w.a, R0);
+          float X[REG];
+          tm_ld32(tm_slot(tb, w.b), X);
+          tm_st32(tm_slot(tb, w.a), X);
         }
         break;
       case OP_BCAST:
-        row_cross_read();
-#pragma unroll
-        for (int v = 0; v < NV; v++) {
-          const float x0 = RB[L.row[v] & (kMaxRows - 1)];
-#pragma unroll
-          for (int e = 0; e < VE; e++) R0[v * VE + e] = x0;
-        }
+        bcast_row<VE>(A, Q0);
         break;
       case OP_ADD: case OP_SUB: case OP_MUL: case OP_DIV: case OP_MAX: case OP_MIN: case OP_POW: {
         const bool rev = fl & CF_REV;
         const bool ar = fl & CF_AROW, xr = fl & CF_XROW, imm = fl & CF_IMM;
+        const float xi = __uint_as_float(w.imm);
         if (ar && (xr || imm)) {
-          // ROW op ROW -> ROW, in the ACC row buffer (owner threads)
-          row_write_begin();
-          const float xi = __uint_as_float(w.imm);
-          const float* xrow = RB + w.a * kMaxRows;
-          DVM_ROWS_FOR(r) {
-            const float a0 = RB[r];
-            const float x0 = imm ? xi : xrow[r];
-            RB[r] = rev ? bin_rt(w.op, x0, a0) : bin_rt(w.op, a0, x0);
-          }
-          row_write_end();
+          // ROW op ROW -> ROW
+          row_binary(w.op, rev, Q0, xr ? rowslot(w.a, warp) : nullptr, xi, nvr);
+          if (P.ur) row_fill(Q0, NV);
           break;
         }
         if (w.op == OP_DIV || w.op == OP_POW) {
-          if (ar || xr) row_cross_read();
-          if (!ar) slot_write(3, R0);
-          heavy_binary_loop<VE>(w.op, rev, ar, xr ? RB + w.a * kMaxRows : nullptr, imm ? -1 : (int)w.a,
-                                __uint_as_float(w.imm), P.m);
-          slot_read(3, R0);
+          // FULL result through the scratch register
+          if (ar) bcast_row<VE>(A, Q0);
+          uint32_t xcol = 0;
+          if (!xr && !imm) {
+            if (w.a == 0) {
+              tm_st32(tm_slot(tb, 1) + 96u, A);  // X = ACC itself: a copy next to the scratch
+              xcol = tm_slot(tb, 1) + 96u;
+            } else {
+              xcol = tm_slot(tb, w.a);
+            }
+          }
+          tm_st32(tm_scratch(tb), A);
+          heavy_binary_loop(w.op, rev, tm_scratch(tb), !xr && !imm, xcol, xr ? rowslot(w.a, warp) : nullptr, xi, VE);
+          tm_ld32(tm_scratch(tb), A);
           break;
         }
-        switch (w.op) {
-          DVM_BIN_CASE(OP_ADD) DVM_BIN_CASE(OP_SUB) DVM_BIN_CASE(OP_MUL)
-          DVM_BIN_CASE(OP_MAX) DVM_BIN_CASE(OP_MIN)
-          default: break;
+        // light ops: the operand is an immediate, a ROW area, ACC, or a slot from TMEM
+        if (imm || xr) {
+          float xv[NV];
+          const float* xrow = rowslot(w.a, warp);
+#pragma unroll
+          for (int v = 0; v < NV; v++) xv[v] = imm ? xi : xrow[v];
+          switch (w.op) {
+            case OP_ADD: bin_fv<VE, OP_ADD>(A, xv, rev); break;
+            case OP_SUB: bin_fv<VE, OP_SUB>(A, xv, rev); break;
+            case OP_MUL: bin_fv<VE, OP_MUL>(A, xv, rev); break;
+            case OP_MAX: bin_fv<VE, OP_MAX>(A, xv, rev); break;
+            default: bin_fv<VE, OP_MIN>(A, xv, rev); break;
+          }
+          break;
+        }
+        float X[REG];
+        if (w.a == 0) {
+#pragma unroll
+          for (int e = 0; e < REG; e++) X[e] = A[e];
+        } else {
+          tm_ld32(tm_slot(tb, w.a), X);
+        }
+        if (ar) {
+          float av[NV];
+#pragma unroll
+          for (int v = 0; v < NV; v++) av[v] = Q0[v];
+          switch (w.op) {
+            case OP_ADD: bin_vf<VE, OP_ADD>(A, av, X, rev); break;
+            case OP_SUB: bin_vf<VE, OP_SUB>(A, av, X, rev); break;
+            case OP_MUL: bin_vf<VE, OP_MUL>(A, av, X, rev); break;
+            case OP_MAX: bin_vf<VE, OP_MAX>(A, av, X, rev); break;
+            default: bin_vf<VE, OP_MIN>(A, av, X, rev); break;
+          }
+        } else {
+          switch (w.op) {
+            case OP_ADD: bin_ff<OP_ADD>(A, X, rev); break;
+            case OP_SUB: bin_ff<OP_SUB>(A, X, rev); break;
+            case OP_MUL: bin_ff<OP_MUL>(A, X, rev); break;
+            case OP_MAX: bin_ff<OP_MAX>(A, X, rev); break;
+            default: bin_ff<OP_MIN>(A, X, rev); break;
+          }
         }
         break;
       }
       case OP_RSUM:
       case OP_RMAX: {
-        // ACC (FULL) -> ACC row buffer.  Fixed order: each thread combines its vectors of
-        // one row in order, the warp butterfly combines the lanes, then the row's owner
-        // thread adds the warps' partials in warp order.
+        // ACC (FULL) -> ACC (ROW).  Fixed order: each thread combines its vectors of one
+        // row in order, the warp butterfly combines the lanes, then every thread of the
+        // row adds the warps' (or segments') partials in order.
         const bool mx = w.op == OP_RMAX;
         const float ident = mx ? -INFINITY : 0.f;
-        if (row_dirty || row_read) __syncthreads();  // red[] of an earlier reduction may still be read
-        float run = ident;
-#pragma unroll
-        for (int v = 0; v < NV; v++) {
-          if (!((L.seg >> v) & 1u)) continue;
+        float* red = red_buf(rbuf);
+        rbuf ^= 1;
+        if (P.ur) {
           float p = ident;
-          if ((L.rowok >> v) & 1u) {
-            const int nc = ncol<VE>(P, O, L, v);
 #pragma unroll
-            for (int e = 0; e < VE; e++)
-              if (e < nc) p = mx ? vmax(p, R0[v * VE + e]) : p + R0[v * VE + e];
+          for (int v = 0; v < NV; v++) {
+            if (!((L.seg >> v) & 1u)) continue;
+            if ((L.rowok >> v) & 1u) {
+              const int nc = ncol<VE>(P, O, L, v);
+              float s0 = ident, s1 = ident;
+              if (nc == VE) {
+#pragma unroll
+                for (int e = 0; e < VE; e += 2) {
+                  s0 = mx ? vmax(s0, A[v * VE + e]) : s0 + A[v * VE + e];
+                  s1 = mx ? vmax(s1, A[v * VE + e + 1]) : s1 + A[v * VE + e + 1];
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < VE; e++)
+                  if (e < nc) s0 = mx ? vmax(s0, A[v * VE + e]) : s0 + A[v * VE + e];
+              }
+              const float s = mx ? vmax(s0, s1) : s0 + s1;
+              p = mx ? vmax(p, s) : p + s;
+            }
           }
-          run = mx ? vmax(run, p) : run + p;
-          const bool last = v == NV - 1 || !((L.seg >> (v + 1)) & 1u) || L.row[v + 1] != L.row[v];
-          if (last) {
-            const float q = mx ? warp_reduce<true>(run) : warp_reduce<false>(run);
-            if (lane == 0) red_buf()[L.row[v] * NW + warp] = q;
-            run = ident;
-          }
-        }
-        __syncthreads();
-        DVM_ROWS_FOR(r) {
-          const int nwc = P.m < NW ? P.m : NW;
+          p = mx ? warp_reduce<true>(p) : warp_reduce<false>(p);
+          if (lane == 0 && L.seg) red[warp] = p;
+          consumer_sync();
           float q = ident;
-          for (int j = 0; j < nwc; j++) {
-            const float x = red_buf()[r * NW + ((r * P.m + j) % NW)];
-            q = mx ? vmax(q, x) : q + x;
+          if (L.seg)
+            for (int k = L.rw0; k < L.rw1; k++) q = mx ? vmax(q, red[k]) : q + red[k];
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < NV; v++) Q0[v] = q;
+          __syncwarp();
+        } else {
+          // general: one butterfly per segment, then each row's segments in order
+#pragma unroll
+          for (int v = 0; v < NV; v++) {
+            if (!((L.seg >> v) & 1u)) continue;   // warp-uniform
+            float p = ident;
+            if ((L.rowok >> v) & 1u) {
+              const int nc = ncol<VE>(P, O, L, v);
+#pragma unroll
+              for (int e = 0; e < VE; e++)
+                if (e < nc) p = mx ? vmax(p, A[v * VE + e]) : p + A[v * VE + e];
+            }
+            p = mx ? warp_reduce<true>(p) : warp_reduce<false>(p);
+            if (lane == 0) red[warp * P.nvu + v] = p;
           }
-          RB[r] = q;
+          consumer_sync();
+          __syncwarp();
+#pragma unroll 1
+          for (int v = 0; v < NV; v++) {
+            float q = ident;
+            if ((L.seg >> v) & 1u) {
+              const int s0 = L.row(v) * P.m;
+              for (int k = 0; k < P.m; k++) q = mx ? vmax(q, red[s0 + k]) : q + red[s0 + k];
+            }
+            Q0[v] = q;
+          }
+          __syncwarp();
         }
-        row_read = false;
-        row_dirty = true;
         break;
       }
       case OP_ASUM:
         if (fl & CF_AROW) {
-          if (threadIdx.x < (unsigned)P.rows) {
-            int64_t off;
-            const int64_t zero4[4] = {0, 0, 0, 0};
-            if (row_off(P, O, threadIdx.x, zero4, off)) grand += RB[threadIdx.x];
+          // one value per row: the thread holding the row's first segment (lane 0)
+#pragma unroll 1
+          for (int v = 0; v < NV; v++) {
+            const int s = warp * P.nvu + v;
+            if (lane == 0 && ((L.rowok >> v) & 1u) && s % P.m == 0) grand += Q0[v];
           }
         } else {
 #pragma unroll
@@ -1067,7 +1157,7 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
               const int nc = ncol<VE>(P, O, L, v);
 #pragma unroll
               for (int e = 0; e < VE; e++)
-                if (e < nc) grand += R0[v * VE + e];
+                if (e < nc) grand += A[v * VE + e];
             }
         }
         break;
@@ -1075,18 +1165,17 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
       case OP_ISFIN: case OP_NEG: case OP_RSQRT: case OP_RECIP: case OP_SILU: case OP_CASTBF: {
         const int op = w.op;
         if (fl & CF_AROW) {
-          row_write_begin();
-          DVM_ROWS_FOR(r) RB[r] = unary_fn(op, RB[r]);
-          row_write_end();
+          row_unary(op, Q0, nvr);
+          if (P.ur) row_fill(Q0, NV);
         } else if (heavy_unary(op)) {
-          slot_write(3, R0);
-          heavy_unary_loop(op);
-          slot_read(3, R0);
+          tm_st32(tm_scratch(tb), A);
+          heavy_unary_loop(op, tm_scratch(tb));
+          tm_ld32(tm_scratch(tb), A);
         } else {
           switch (op) {  // light ops: one unrolled register loop per opcode
 #define DVM_UNARY_CASE(OPC)                                                        \
   case OPC:                                                                        \
-    _Pragma("unroll") for (int e = 0; e < REG; e++) R0[e] = unary_fn(OPC, R0[e]); \
+    _Pragma("unroll") for (int e = 0; e < REG; e++) A[e] = unary_fn(OPC, A[e]);    \
     break;
             DVM_UNARY_CASE(OP_ABS) DVM_UNARY_CASE(OP_ROUND) DVM_UNARY_CASE(OP_FLOOR) DVM_UNARY_CASE(OP_ISFIN)
             DVM_UNARY_CASE(OP_NEG) DVM_UNARY_CASE(OP_CASTBF)
@@ -1102,22 +1191,20 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
     }
   }
 }
-#undef DVM_ROWS_FOR
-#undef DVM_BIN_CASE
 
 // ---- grid-wide sum (GSUM) -------------------------------------------------
-// Called by every thread of the CTA.  The result is identical on every CTA (fixed
-// combination order).  The wait for the other CTAs is bounded; on expiry the status
-// word is set and every thread of the CTA sees `abort`.
+// Called by every thread of the CTA.  The result is
+// identical on every CTA (fixed combination order).  The wait for the other CTAs is
+// bounded; on expiry the status word is set and every thread of the CTA sees `abort`.
 __device__ __forceinline__ float grid_sum(const LaunchParams& Pm, float grand, int lane) {
   const int warp = threadIdx.x >> 5;
   __syncthreads();
   const float p = warp_reduce<false>(grand);
-  if (lane == 0) red_buf()[warp] = p;
+  if (lane == 0) cta_partials()[warp] = p;
   __syncthreads();
   if (threadIdx.x == 0) {
     float cta = 0.f;
-    for (int w = 0; w < NW; w++) cta += red_buf()[w];
+    for (int w = 0; w < NW; w++) cta += cta_partials()[w];
     Pm.partials[blockIdx.x] = cta;
     __threadfence();
     if (!(Pm.skip_arrival && blockIdx.x == 0)) atomicAdd(Pm.barrier, 1ull);
@@ -1146,7 +1233,76 @@ __device__ __forceinline__ float grid_sum(const LaunchParams& Pm, float grand, i
   return *misc_scalar();
 }
 
+// ---- the producer (thread 0) -------------------------------------------------
+// Issue staged tiles ahead of the consumers.  Tiles up to index `need` (exclusive) are
+// required now and waited for; further ones, up to `limit`, are issued only while their
+// stage is already free, so thread 0 never waits on slower warps without need.
+__device__ __forceinline__ void issue_upto(const LaunchParams& Pm, const uint8_t* img, const Ctl& C, int a, int need,
+                                           int limit, bool plain) {
+  Issuer& I = issuer();
+  while (I.issued < limit && !*abort_flag()) {
+    if (plain) {
+      while (true) {
+        if (I.g >= I.g_end) return;
+        const ProgRec* pr = reinterpret_cast<const ProgRec*>(img + sizeof(Header) + I.prog * sizeof(ProgRec));
+        const int end = (int)(pr->tile_base + pr->block_dim);
+        if (I.g >= end) {  // the current program is done: set up the next one
+          I.prog++;
+          Prog Q;
+          load_prog(img, I.prog, Q, a);
+          dma_section(I, Q, Pm, Q.body + 1, (int)Q.body[0].imm);
+          I.tau = I.g - (int)Q.pr->tile_base;
+          I.c0 = I.tau / Q.tiles_in;
+          I.cin = I.tau - I.c0 * Q.tiles_in;
+          continue;
+        }
+        if (!I.stage_sec) {  // nothing to stage in this program: skip its tiles
+          I.g = end;
+          continue;
+        }
+        break;
+      }
+    } else if (I.tau >= I.t_end || !I.stage_sec) {
+      return;
+    }
+    const int stage = I.issued % C.n_stages;
+    const uint32_t parity = ((I.issued / C.n_stages) & 1) ^ 1;
+    if (I.issued >= need) {
+      if (!mbar_try_wait(bar_empty(stage), parity)) return;  // not free yet: try again next tile
+    } else if (!mbar_wait(bar_empty(stage), parity, C.st, abort_flag())) {
+      return;
+    }
+    // tile origin from the cached geometry (rank <= 2 incrementally, else by division)
+    int od[3] = {0, 0, 0};
+    int oin;
+    if (I.r <= 2) {
+      od[0] = I.r == 2 ? I.c0 * I.t0 : 0;
+      oin = I.cin * I.t_in;
+    } else {
+      int tau = I.tau;
+      oin = (tau % I.tiles_in) * I.t_in;
+      tau /= I.tiles_in;
+      for (int dd = I.r - 2; dd >= 0; dd--) {
+        const int td = (int)((I.pr->n[dd] + I.pr->t[dd] - 1) / I.pr->t[dd]);
+        od[dd] = (tau % td) * (int)I.pr->t[dd];
+        tau /= td;
+      }
+    }
+    issue_tile(I, od[0], od[1], od[2], oin, dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes, bar_full(stage));
+    I.issued++;
+    I.tau++;
+    if (++I.cin == I.tiles_in) {
+      I.cin = 0;
+      I.c0++;
+    }
+    if (plain) I.g++;
+  }
+}
+
 // ---- the kernel --------------------------------------------------------------
+// One walk over the CTA's work with a single tile-execution site: plain and stacked
+// launches over the concatenated tile range [lo, hi) across programs, sectioned
+// programs over their top-level control flow (TILES / GSUM / SST / JLE0 / JMP / END).
 template <int VE>
 __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_constant__ LaunchParams Pm) {
   uint8_t* smem = dvm_smem;
@@ -1166,6 +1322,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
     }
     mbar_init(bar_hoist(), 1);
     *abort_flag() = 0;
+    issuer().issued = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -1186,38 +1343,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
   const int n_progs = H->n_progs;
 
   // hoisted (tile-invariant) loads: once per CTA, all programs, one mbarrier phase
-  if (tid == 0 && has_work) {
+  if (tid == 0 && has_work && H->hoist_bytes) {
     uint32_t total = 0;
-    TilePos O0;
-    O0.tau = O0.c0 = O0.cin = 0;
-    O0.od[0] = O0.od[1] = O0.od[2] = 0;
-    O0.oin = 0;
     for (int mode = 0; mode < 2; mode++) {
       if (mode == 1) mbar_arrive_expect_tx(bar_hoist(), total);
-      if (!H->hoist_bytes) continue;
       for (int p = 0; p < n_progs; p++) {
         Prog P;
         load_prog(smem, p, P, a);
-        total += dma_tile(Pm, P, P.body, (int)P.pr->body_len, O0, hoist_area() + P.pr->hoist_base, bar_hoist(),
-                          true, mode);
+        total += dma_hoist(Pm, P, hoist_area() + P.pr->hoist_base, bar_hoist(), mode);
       }
     }
   }
   if (H->hoist_bytes && has_work) mbar_wait(bar_hoist(), 0, C.st, abort_flag());
 
-  float R0[REG];
+  // TMEM: the slots and scratch registers (warp 0 allocates and frees all columns)
+  if (warp == 0) {
+    tc_alloc(smem_u32(dvm_smem + kTmemOff), kTmemCols);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tm_base(*reinterpret_cast<volatile uint32_t*>(dvm_smem + kTmemOff));
+
+  float A[REG];
 #pragma unroll
-  for (int e = 0; e < REG; e++) R0[e] = 0.f;
+  for (int e = 0; e < REG; e++) A[e] = 0.f;
   float grand = 0.f;
-  bool row_read = false, row_dirty = false;
+  int rbuf = 0;
   int it = 0;  // staged tiles consumed
   Lanes<VE> L;
   Prog P;
   TilePos T;
 
-  // One walk over the CTA's work, with a single tile-execution site:
-  //   plain/stacked — the concatenated tile range [lo, hi) across programs;
-  //   sectioned     — the top-level control flow (TILES / GSUM / SST / JLE0 / JMP / END).
   int p = -1;        // plain: current program
   int g = lo;        // plain: next concatenated tile
   int pc = 0;        // sectioned: next top-level instruction
@@ -1230,7 +1388,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
     p = 0;
     load_prog(smem, 0, P, a);
     lanes_for_prog<VE>(P, warp, lane, L);
-    fill_rowcoords(P);
+    fill_tables<VE>(P);
   }
   while (true) {
     if (!sectioned) {
@@ -1242,7 +1400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
           p++;
         load_prog(smem, p, P, a);
         lanes_for_prog<VE>(P, warp, lane, L);
-        fill_rowcoords(P);
+        fill_tables<VE>(P);
         sec = P.body + 1;
         sec_n = (int)P.body[0].imm;
         staged = section_has_stage(sec, sec_n);
@@ -1253,14 +1411,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
           I.prog = p;
           I.g = g;
           I.g_end = hi;
-          I.sec_off = (int)(P.pr->body_off / sizeof(Instr)) + 1;
-          I.sec_n = sec_n;
-          issuer_section(I, P, Pm, sec, sec_n);
+          dma_section(I, P, Pm, sec, sec_n);
           I.tau = tau;
           I.c0 = T.c0;
           I.cin = T.cin;
           I.issued = 0;
-          issue_upto(Pm, smem, C, a, C.n_stages ? C.n_stages - 1 : 0, true);
         }
       }
     } else {
@@ -1283,20 +1438,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
             if (tid == 0 && staged) {
               Issuer& I = issuer();
               I.prog = 0;
-              I.sec_off = (int)(P.pr->body_off / sizeof(Instr)) + (int)(sec - P.body);
-              I.sec_n = sec_n;
-              issuer_section(I, P, Pm, sec, sec_n);
+              dma_section(I, P, Pm, sec, sec_n);
               I.tau = tau;
               I.t_end = t_end;
               I.c0 = T.c0;
               I.cin = T.cin;
               I.issued = it;
-              issue_upto(Pm, smem, C, a, it + C.n_stages - 1, false);
             }
           }
         } else if (w.op == OP_GSUM) {
           S = grid_sum(Pm, grand, lane);
-          row_read = row_dirty = false;
           if (*abort_flag()) {
             done = true;
             break;
@@ -1319,12 +1470,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
       }
       if (done) break;
     }
-    if (staged && tid == 0) issue_upto(Pm, smem, C, a, it + C.n_stages, !sectioned);
-    exec_tile<VE>(Pm, P, sec, sec_n, T, L, lane, it, C, grand, R0, row_read, row_dirty);
+    if (staged && tid == 0) issue_upto(Pm, smem, C, a, it + 1, it + C.n_stages, !sectioned);
+    exec_tile<VE>(Pm, P, sec, sec_n, T, L, lane, it, C, grand, A, rbuf, tb);
     if (staged) it++;
     pos_next(P, T);
     if (sectioned) tau++;
     else g++;
+  }
+  // copies still in flight land before the CTA exits (after an abort the consumers may
+  // not have waited for them)
+  if (tid == 0 && C.n_stages) {
+    const int issued = issuer().issued;
+    for (int j = issued > C.n_stages ? issued - C.n_stages : 0; j < issued; j++) {
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait_sleep(bar_full(j % C.n_stages), (uint32_t)((j / C.n_stages) & 1), 20000u))
+        if (globaltimer() - t0 > C.st.limit_ns) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tc_dealloc(*reinterpret_cast<volatile uint32_t*>(dvm_smem + kTmemOff), kTmemCols);
   }
 }
 
