@@ -52,8 +52,9 @@ constexpr int kSegOff = kRowCoordOff + kMaxRows * 16;     // per segment: tile r
 constexpr int kMiscOff = kSegOff + kMaxSegs * 4;          // grid-sum result, abort flag, CTA partials
 constexpr int kIssOff = kMiscOff + 128;                   // producer state (thread 0)
 constexpr int kRowSlotOff = kIssOff + 384;                // ROW values of ACC, slots 1, 2: [slot][warp][8]
-constexpr int kTmemOff = kRowSlotOff + 3 * NW * 8 * 4;    // TMEM base address
-constexpr int kDataOff = kTmemOff + 128;                  // hoist area, then the stage ring
+constexpr int kTmemOff = kRowSlotOff + 3 * NW * 8 * 4;    // TMEM base address (ROW areas: 8 values per warp)
+constexpr int kUopOff = kTmemOff + 128;                   // decoded micro-ops of the current section
+constexpr int kDataOff = kUopOff + kMaxInstr * 16;        // hoist area, then the stage ring
 static_assert(kDataOff % 128 == 0, "data area alignment");
 static_assert(kDataOff + kSmemBudget <= 227 * 1024, "shared memory of the VEC interpreter");
 
@@ -306,42 +307,46 @@ __device__ __forceinline__ void dma_section(Issuer& D, const Prog& P, const Laun
 }
 
 // one staged tile at origin (od0..od2, oin): arm the full barrier with the byte count,
-// then issue the copies
-__device__ __forceinline__ void issue_tile(const Issuer& D, int od0, int od1, int od2, int o_in, uint8_t* dst_base,
+// then issue the copies.  The issuer state is read into registers first: the copy
+// instructions clobber memory, which would otherwise make every field a new load.
+__device__ __forceinline__ void issue_tile(const Issuer& Ds, int od0, int od1, int od2, int o_in, uint8_t* dst_base,
                                            uint64_t* bar) {
-  const int valid_in = min(D.t_in, D.n_in - o_in);
-  const int nrows = D.r == 2 ? min(D.rows, D.n0 - od0) : 1;
+  const int n = Ds.n, r = Ds.r, t_in = Ds.t_in, rows = Ds.rows;
+  const ProgRec* pr = Ds.pr;
+  const TensRec* tens = Ds.tens;
+  const int valid_in = min(t_in, Ds.n_in - o_in);
+  const int nrows = r == 2 ? min(rows, Ds.n0 - od0) : 1;
   for (int mode = 0; mode < 2; mode++) {
     uint32_t total = 0;
-    for (int k = 0; k < D.n; k++) {
-      const DmaEnt& e = D.e[k];
+    for (int k = 0; k < n; k++) {
+      const DmaEnt e = Ds.e[k];  // a copy: its fields stay in registers
       uint8_t* dst = dst_base + e.aux0;
       const uint32_t rowb = (uint32_t)(valid_in * e.esz);
-      if (e.kind == 0) {  // one row shared by the tile (outer strides 0 within the tile)
+      if (e.kind == 1 && valid_in == t_in) {  // whole rows: one contiguous block
+        const uint32_t bytes = (uint32_t)nrows * t_in * e.esz;
+        total += bytes;
+        if (mode) bulk_g2s(dst, e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz, bytes, bar);
+      } else if (e.kind == 0) {  // one row shared by the tile (outer strides 0 within the tile)
         int64_t off = 0;
         bool ok = true;
-        if (D.r > 2) ok = row_off_div(D.pr, D.r, od0, od1, od2, 0, D.tens[e.tens].vs, &off);
+        if (r > 2) ok = row_off_div(pr, r, od0, od1, od2, 0, tens[e.tens].vs, &off);
         else off = (int64_t)od0 * e.vs0;
         if (ok) {
           total += rowb;
           if (mode) bulk_g2s(dst, e.src + (off + o_in) * e.esz, rowb, bar);
         }
-      } else if (e.kind == 1 && valid_in == D.t_in) {  // whole rows: one contiguous block
-        const uint32_t bytes = (uint32_t)nrows * D.t_in * e.esz;
-        total += bytes;
-        if (mode) bulk_g2s(dst, e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz, bytes, bar);
       } else if (e.kind <= 2) {  // rank <= 2, row by row
         const uint8_t* src = e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz;
         total += rowb * nrows;
         if (mode)
           for (int row = 0; row < nrows; row++)
-            bulk_g2s(dst + (size_t)row * D.t_in * e.esz, src + (int64_t)row * e.vs0 * e.esz, rowb, bar);
+            bulk_g2s(dst + (size_t)row * t_in * e.esz, src + (int64_t)row * e.vs0 * e.esz, rowb, bar);
       } else {  // rank > 2
-        for (int row = 0; row < D.rows; row++) {
+        for (int row = 0; row < rows; row++) {
           int64_t off;
-          if (!row_off_div(D.pr, D.r, od0, od1, od2, row, D.tens[e.tens].vs, &off)) continue;
+          if (!row_off_div(pr, r, od0, od1, od2, row, tens[e.tens].vs, &off)) continue;
           total += rowb;
-          if (mode) bulk_g2s(dst + (size_t)row * D.t_in * e.esz, e.src + (off + o_in) * e.esz, rowb, bar);
+          if (mode) bulk_g2s(dst + (size_t)row * t_in * e.esz, e.src + (off + o_in) * e.esz, rowb, bar);
         }
       }
     }
@@ -365,10 +370,9 @@ struct Lanes {
 };
 
 // fill the row-coordinate table (rank > 2) and the segment table of a program (all
-// threads call it when the CTA switches program)
+// threads call it when the CTA switches program, between two CTA barriers)
 template <int VE>
 __device__ __forceinline__ void fill_tables(const Prog& P) {
-  __syncthreads();  // the previous program's tiles may still read the tables
   const int a = VE * 32;
   for (int s = threadIdx.x; s < P.segs; s += NCT)
     reinterpret_cast<int*>(dvm_smem + kSegOff)[s] = ((s / P.m) << 16) | ((s % P.m) * a);
@@ -383,7 +387,6 @@ __device__ __forceinline__ void fill_tables(const Prog& P) {
       }
     }
   }
-  __syncthreads();
 }
 
 // Segments (512-byte runs of one tile row) are dealt to warps in blocks: warp w holds
@@ -433,10 +436,13 @@ __device__ __forceinline__ int ncol(const Prog& P, const TilePos& O, const Lanes
 
 // ---- tensor memory -------------------------------------------------------------
 // Each CTA allocates all 512 TMEM columns.  Warp w may access lanes 32*(w%4)..+31; the
-// warps w and w+4 share those lanes and split the columns.  Per thread: slot 1 at
-// columns [0, 32), slot 2 at [32, 64), the scratch register at [64, 96) and a spare
-// register at [96, 128) of its half.
+// NW/4 warps that share those lanes split the columns into blocks of kTmemPerThread.
+// In a thread's block, in units of one FULL register (REG columns): slot 1, slot 2,
+// the scratch register, a spare register, then kHoistCache hoisted-load cache registers.
 constexpr uint32_t kTmemCols = 512;
+constexpr int kTmemPerThread = 512 / (NW / 4);
+constexpr int kHoistCache = kTmemPerThread / REG - 4;
+static_assert(kHoistCache >= 0, "TMEM layout of the VEC interpreter");
 __device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
 }
@@ -451,15 +457,17 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 __device__ __forceinline__ uint32_t tm_base(uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
-  return tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 256);
+  return tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * kTmemPerThread);
 }
-__device__ __forceinline__ uint32_t tm_slot(uint32_t tb, int k) { return tb + (uint32_t)(k - 1) * 32u; }
-__device__ __forceinline__ uint32_t tm_scratch(uint32_t tb) { return tb + 64u; }
+__device__ __forceinline__ uint32_t tm_slot(uint32_t tb, int k) { return tb + (uint32_t)((k - 1) * REG); }
+__device__ __forceinline__ uint32_t tm_scratch(uint32_t tb) { return tb + 2u * REG; }
+__device__ __forceinline__ uint32_t tm_spare(uint32_t tb) { return tb + 3u * REG; }
+__device__ __forceinline__ uint32_t tm_hoist(uint32_t tb, int k) { return tb + (uint32_t)((4 + k) * REG); }
 
 // 32 columns of this thread's lane <-> 32 registers; each access waits for its own
 // completion (the wait is in the same statement, so no use of the registers can be
 // scheduled before the data is there, and no later access can overtake a store)
-__device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[REG]) {
+__device__ __forceinline__ void tm_ld32w(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -474,7 +482,7 @@ __device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[REG]) {
 #pragma unroll
   for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[REG]) {
+__device__ __forceinline__ void tm_st32w(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
       "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
@@ -488,6 +496,38 @@ __device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[REG]) {
       "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
       "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+}
+// 16 columns <-> 16 registers (the same, for a FULL register of 16 values)
+__device__ __forceinline__ void tm_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+// one FULL register (REG values) of this thread <-> TMEM
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[REG]) {
+  if constexpr (REG == 32) tm_ld32w(taddr, v);
+  else tm_ld16(taddr, v);
+}
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[REG]) {
+  if constexpr (REG == 32) tm_st32w(taddr, v);
+  else tm_st16(taddr, v);
 }
 __device__ __forceinline__ float4 tm_ld4(uint32_t taddr) {
   uint32_t a, b, c, d;
@@ -569,60 +609,6 @@ __device__ __forceinline__ void ldg_vectors_fast(float (&dst)[REG], const uint8_
   }
 }
 
-// LD of a FULL value
-template <int VE>
-__device__ __forceinline__ void op_load(float (&dst)[REG], const Instr& w, const Prog& P, const Lanes<VE>& L,
-                                        const TilePos& O, const LaunchParams& Pm, const uint8_t* stage_base,
-                                        uint32_t tb) {
-  const TensRec& T = P.tens[w.b];
-  const int dt = T.dtype;
-  if (w.flags & LF_DMA) {
-    const uint8_t* region = ((w.flags & LF_HOIST) ? hoist_area() + P.pr->hoist_base : stage_base) + w.aux0;
-    const int rstride = (w.flags & LF_COLV) ? 0 : P.t_in;
-    if (dt == DT_F32) {
-      lds_vectors<VE, 4>(dst, region, rstride, L);
-    } else if (dt == DT_BF16) {
-      if constexpr (VE >= 8) lds_vectors<VE, 2>(dst, region, rstride, L);
-    } else {
-      if constexpr (VE == 16) lds_vectors<VE, 1>(dst, region, rstride, L);
-    }
-    return;
-  }
-  const uint8_t* base = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
-  const int64_t vin = T.vs[P.r - 1];
-  const int esz = dtype_size(dt);
-  // full-tile fast path: every valid vector complete, rows inside, 16-byte aligned rows
-  const bool mine = P.r <= 2 && vin == 1 && L.rowok == L.seg && O.oin + P.t_in <= P.n_in &&
-                    (((P.r == 2 ? T.vs[0] : 0) * esz) & 15) == 0;
-  if (__all_sync(0xffffffffu, mine)) {
-    const int64_t vs0 = P.r == 2 ? T.vs[0] : 0;
-    if (dt == DT_F32) {
-      ldg_vectors_fast<VE, 4>(dst, base, vs0, O.oin, O, L);
-    } else if (dt == DT_BF16) {
-      if constexpr (VE >= 8) ldg_vectors_fast<VE, 2>(dst, base, vs0, O.oin, O, L);
-    } else {
-      if constexpr (VE == 16) ldg_vectors_fast<VE, 1>(dst, base, vs0, O.oin, O, L);
-    }
-    return;
-  }
-  // general masked path (ragged tails, strided views, rank > 2): a rolled loop through
-  // the TMEM scratch register keeps it compact
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-#pragma unroll 1
-  for (int j = 0; j < REG; j++) {
-    const int v = j / VE, e = j % VE;
-    const int s = warp * P.nvu + v;
-    const int row = s / P.m, col = (s % P.m) * (VE * 32) + lane * VE;
-    float x = 0.f;
-    int64_t off;
-    if (v < P.nvu && s < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
-      x = load_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt);
-    tm_st1(tm_scratch(tb) + (uint32_t)j, x);
-  }
-  tm_ld32(tm_scratch(tb), dst);
-}
-
 // ---- stores from ACC --------------------------------------------------------
 __device__ __forceinline__ void store_scalar(uint8_t* base, int64_t off, int dt, float x) {
   if (dt == DT_F32) reinterpret_cast<float*>(base)[off] = x;
@@ -662,42 +648,6 @@ __device__ __forceinline__ void stg_vectors_fast(const float (&acc)[REG], uint8_
     if (!((L.seg >> v) & 1u)) continue;
     const int64_t off = (int64_t)(O.od[0] + L.row(v)) * vs0 + oin + L.col(v);
     pack_store<VE, ESZ>(base + off * ESZ, acc + v * VE);
-  }
-}
-
-template <int VE>
-__device__ __forceinline__ void op_store(const float (&acc)[REG], const Instr& w, const Prog& P, const Lanes<VE>& L,
-                                         const TilePos& O, const LaunchParams& Pm, uint32_t tb) {
-  const TensRec& T = P.tens[w.a];
-  const int dt = T.dtype;
-  const int esz = dtype_size(dt);
-  uint8_t* base = static_cast<uint8_t*>(Pm.ptrs[T.binding]);
-  const int64_t vin = T.vs[P.r - 1];
-  const bool mine = P.r <= 2 && vin == 1 && L.rowok == L.seg && O.oin + P.t_in <= P.n_in &&
-                    (((P.r == 2 ? T.vs[0] : 0) * esz) & 15) == 0;
-  if (__all_sync(0xffffffffu, mine)) {
-    const int64_t vs0 = P.r == 2 ? T.vs[0] : 0;
-    if (dt == DT_F32) {
-      stg_vectors_fast<VE, 4>(acc, base, vs0, O.oin, O, L);
-    } else if (dt == DT_BF16) {
-      if constexpr (VE >= 8) stg_vectors_fast<VE, 2>(acc, base, vs0, O.oin, O, L);
-    } else {
-      if constexpr (VE == 16) stg_vectors_fast<VE, 1>(acc, base, vs0, O.oin, O, L);
-    }
-    return;
-  }
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  tm_st32(tm_scratch(tb), acc);
-#pragma unroll 1
-  for (int j = 0; j < REG; j++) {
-    const int v = j / VE, e = j % VE;
-    const int s = warp * P.nvu + v;
-    const int row = s / P.m, col = (s % P.m) * (VE * 32) + lane * VE;
-    const float x = tm_ld1(tm_scratch(tb) + (uint32_t)j);
-    int64_t off;
-    if (v < P.nvu && s < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
-      store_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt, x);
   }
 }
 
@@ -832,16 +782,13 @@ __device__ __forceinline__ float warp_reduce(float p) {
 }
 
 // ---- heavy math -------------------------------------------------------------
-// Transcendental and correctly rounded ops (sqrt, rsqrt, recip, log, exp, silu, div,
-// pow) are long instruction sequences.  They run as a rolled loop, 4 values per
-// iteration, over the thread's scratch register in TMEM, so each appears once in the
-// interpreter's code.
-__device__ __forceinline__ bool heavy_unary(int op) {
-  return op == OP_SQRT || op == OP_LOG || op == OP_EXP || op == OP_RSQRT || op == OP_RECIP || op == OP_SILU;
-}
+// Rare transcendental forms (log, rsqrt, recip, pow, div with a tensor operand) run as
+// a rolled loop, 4 values per iteration, over the thread's scratch register in TMEM,
+// so each appears once in the code.  The common ones (sqrt, exp, silu) have unrolled
+// register handlers.
 __device__ __forceinline__ float4 splat4(float v) { return make_float4(v, v, v, v); }
 
-// ACC <- op(ACC) through the scratch register
+// scratch <- op(scratch)
 __device__ __forceinline__ void heavy_unary_loop(int op, uint32_t sc) {
 #pragma unroll 1
   for (int q = 0; q < REG / 4; q++) {
@@ -869,37 +816,6 @@ __device__ __forceinline__ void heavy_binary_loop(int op, bool rev, uint32_t sc,
     tm_st4(sc + 4u * q, o);
   }
 }
-// ROW op: one value (one-row programs) or one per vector, in a per-warp ROW area
-__device__ __forceinline__ void row_binary(int op, bool rev, float* dst, const float* xrow, float xi, int nv) {
-  __syncwarp();
-#pragma unroll 1
-  for (int v = 0; v < nv; v++) {
-    const float a = dst[v], x = xrow ? xrow[v] : xi;
-    const float r = rev ? bin_rt(op, x, a) : bin_rt(op, a, x);
-    __syncwarp();
-    dst[v] = r;
-    __syncwarp();
-  }
-}
-__device__ __forceinline__ void row_unary(int op, float* dst, int nv) {
-  __syncwarp();
-#pragma unroll 1
-  for (int v = 0; v < nv; v++) {
-    const float r = unary_fn(op, dst[v]);
-    __syncwarp();
-    dst[v] = r;
-    __syncwarp();
-  }
-}
-
-// ROW values are the same in every lane of a warp; after a one-row update the first
-// value is copied to the thread's other vectors
-__device__ __forceinline__ void row_fill(float* dst, int nv) {
-  __syncwarp();
-  const float r0 = dst[0];
-  for (int v = 1; v < nv; v++) dst[v] = r0;
-  __syncwarp();
-}
 
 template <int VE>
 __device__ __forceinline__ void bcast_row(float (&acc)[REG], const float* qv) {
@@ -911,128 +827,628 @@ __device__ __forceinline__ void bcast_row(float (&acc)[REG], const float* qv) {
   }
 }
 
+// ---- micro-ops ------------------------------------------------------------------
+// Each program section is decoded once per CTA into micro-ops.  A micro-op names one
+// specialised handler (opcode x operand form x element size) and may carry the words
+// around it that need no dispatch of their own (superinstructions):
+//   * a WAIT before a staged load and a REL after the section's last staged load;
+//   * a load into a slot followed by MOV ACC <- slot (the value also goes to ACC);
+//   * a load into a slot followed by a light binary op that reads the slot (the op is
+//     applied right after the load; the slot is written only if a later word reads it);
+//   * MOV slot <- ACC followed by a light binary op that reads the slot (X = ACC);
+//   * CASTBF followed by ST (the store rounds ACC first);
+//   * a row reduction followed by ROW-scalar ops on its result (one-row programs).
+// A tile then costs one dispatch per micro-op, and the handlers are straight-line code.
+enum Handler : uint8_t {
+  H_NOP = 0, H_WAIT, H_REL,
+  H_LD_S4, H_LD_S2, H_LD_S1,   // staged or hoisted load from shared memory, element size 4 / 2 / 1
+  H_LD_H,                      // hoisted load kept in a TMEM cache register after the first tile
+  H_LD_G,                      // load straight from global memory
+  H_LDROW,                     // one value per tile row -> ROW area
+  H_ST, H_STROW,
+  H_MOV_AX, H_MOV_XA, H_MOV_XX, H_MOVROW, H_BCAST,
+  // light binary ops on a FULL ACC; X from a TMEM slot (T), ACC itself (A), an immediate
+  // (I) or a ROW area (R); R* = reversed operands
+  H_ADD_T, H_ADD_A, H_ADD_I, H_ADD_R,
+  H_SUB_T, H_SUB_A, H_SUB_I, H_SUB_R, H_RSUB_T, H_RSUB_I, H_RSUB_R,
+  H_MUL_T, H_MUL_A, H_MUL_I, H_MUL_R,
+  // ACC holds a ROW value, X is a FULL slot: result FULL
+  H_VADD_T, H_VSUB_T, H_VRSUB_T, H_VMUL_T,
+  H_BIN_GEN,                   // every other binary form (MAX, MIN, rare forms)
+  H_ROWBIN, H_ROWUN,           // ROW op ROW / imm, unary on ROW
+  H_DIVPOW,                    // DIV / POW with a FULL result
+  H_SQRT, H_EXP, H_SILU, H_HEAVY_U,
+  H_ABS, H_NEG, H_FLOOR, H_ROUND, H_ISFIN, H_CASTBF,
+  H_RSUM_U, H_RMAX_U, H_RRED_G,
+  H_ASUM, H_ASUM_ROW,
+  H_BAD
+};
+// fusion flags
+enum : uint8_t {
+  UF_WAIT = 1,    // wait for the tile's stage first
+  UF_REL = 2,     // release the tile's stage after the load
+  UF_STORE = 4,   // write the loaded value to slot a
+  UF_TOACC = 8,   // ACC <- the loaded value
+  UF_OP = 16,     // ACC <- ACC op loaded value (op in .op, reversed with UF_REV)
+  UF_REV = 32,
+  UF_SAVE = 64,   // binary ops: slot a <- ACC before the op (the op reads X = ACC)
+  UF_CAST = 128,  // stores: round ACC to bf16 first
+};
+struct alignas(16) Uop {
+  uint8_t h;      // handler
+  uint8_t a;      // dst / X slot, or the tensor of a store
+  uint8_t b;      // tensor of a load, or the source slot of a move
+  uint8_t fl;     // flags of the word
+  float imm;      // immediate operand
+  uint32_t off;   // loads from shared memory: byte offset (stage-relative, or absolute for hoisted)
+  uint8_t op;     // the word's opcode; for UF_OP loads the fused binary opcode
+  uint8_t uf;     // fusion flags
+  uint8_t cnt;    // ROW-scalar micro-ops folded into this one (they follow it)
+  uint8_t aux;    // hoisted loads: element size | cache register << 4
+};
+static_assert(sizeof(Uop) == 16, "micro-op");
+__device__ __forceinline__ Uop* uops() { return reinterpret_cast<Uop*>(dvm_smem + kUopOff); }
+__device__ __forceinline__ int* uop_count() { return reinterpret_cast<int*>(dvm_smem + kMiscOff + 32); }
+
+__device__ __forceinline__ uint8_t light_handler(int op, int form, bool rev) {
+  // form: 0 T, 1 A, 2 I, 3 R, 4 V (ACC ROW, X slot)
+  if (op == OP_ADD) { const uint8_t t[5] = {H_ADD_T, H_ADD_A, H_ADD_I, H_ADD_R, H_VADD_T}; return t[form]; }
+  if (op == OP_MUL) { const uint8_t t[5] = {H_MUL_T, H_MUL_A, H_MUL_I, H_MUL_R, H_VMUL_T}; return t[form]; }
+  if (!rev) { const uint8_t t[5] = {H_SUB_T, H_SUB_A, H_SUB_I, H_SUB_R, H_VSUB_T}; return t[form]; }
+  const uint8_t t[5] = {H_RSUB_T, H_SUB_A, H_RSUB_I, H_RSUB_R, H_VRSUB_T};
+  return t[form];
+}
+
+// one word -> one micro-op (no fusion)
+__device__ __forceinline__ Uop decode_word(const Prog& P, const Instr* body, int i, int& hoisted) {
+  const Instr w = body[i];
+  Uop u;
+  u.h = H_BAD;
+  u.a = w.a;
+  u.b = w.b;
+  u.fl = w.flags;
+  u.imm = __uint_as_float(w.imm);
+  u.off = w.aux0;
+  u.op = w.op;
+  u.uf = 0;
+  u.cnt = 0;
+  u.aux = 0;
+  const bool ar = w.flags & CF_AROW, xr = w.flags & CF_XROW, imm = w.flags & CF_IMM, rev = w.flags & CF_REV;
+  switch (w.op) {
+    case OP_WAIT: u.h = H_WAIT; break;
+    case OP_REL: u.h = H_REL; break;
+    case OP_LD:
+      if (w.flags & LF_ROWV) {
+        u.h = H_LDROW;
+      } else if (w.flags & LF_DMA) {
+        const int esz = dtype_size(P.tens[w.b].dtype);
+        u.h = esz == 4 ? H_LD_S4 : esz == 2 ? H_LD_S2 : H_LD_S1;
+        if (w.flags & LF_HOIST) {
+          u.off = kDataOff + P.pr->hoist_base + w.aux0;
+          if (hoisted < kHoistCache) {
+            u.h = H_LD_H;
+            u.aux = (uint8_t)(esz | (hoisted << 4));
+          }
+          hoisted++;
+        }
+        u.uf = w.a ? UF_STORE : UF_TOACC;
+      } else {
+        u.h = H_LD_G;
+        u.uf = w.a ? UF_STORE : UF_TOACC;
+      }
+      break;
+    case OP_ST: u.h = (w.flags & LF_ROWV) ? H_STROW : H_ST; break;
+    case OP_MOV:
+      if (w.flags & 1) u.h = H_MOVROW;
+      else if (w.a == 0) u.h = w.b == 0 ? H_NOP : H_MOV_AX;
+      else u.h = w.b == 0 ? H_MOV_XA : H_MOV_XX;
+      break;
+    case OP_BCAST: u.h = H_BCAST; break;
+    case OP_ADD: case OP_SUB: case OP_MUL: case OP_DIV: case OP_MAX: case OP_MIN: case OP_POW: {
+      if (ar && (xr || imm)) { u.h = H_ROWBIN; break; }
+      if (w.op == OP_DIV || w.op == OP_POW) { u.h = H_DIVPOW; break; }
+      if (w.op == OP_MAX || w.op == OP_MIN) { u.h = H_BIN_GEN; break; }
+      int form;
+      if (ar) {
+        if (w.a == 0) { u.h = H_BIN_GEN; break; }
+        form = 4;
+      } else {
+        form = imm ? 2 : xr ? 3 : (w.a == 0 ? 1 : 0);
+      }
+      u.h = light_handler(w.op, form, rev);
+      break;
+    }
+    case OP_RSUM: u.h = P.ur ? H_RSUM_U : H_RRED_G; break;
+    case OP_RMAX: u.h = P.ur ? H_RMAX_U : H_RRED_G; break;
+    case OP_ASUM: u.h = ar ? H_ASUM_ROW : H_ASUM; break;
+    case OP_SQRT: case OP_ABS: case OP_LOG: case OP_EXP: case OP_ROUND: case OP_FLOOR:
+    case OP_ISFIN: case OP_NEG: case OP_RSQRT: case OP_RECIP: case OP_SILU: case OP_CASTBF:
+      if (ar) { u.h = H_ROWUN; break; }
+      switch (w.op) {
+        case OP_SQRT: u.h = H_SQRT; break;
+        case OP_EXP: u.h = H_EXP; break;
+        case OP_SILU: u.h = H_SILU; break;
+        case OP_ABS: u.h = H_ABS; break;
+        case OP_NEG: u.h = H_NEG; break;
+        case OP_FLOOR: u.h = H_FLOOR; break;
+        case OP_ROUND: u.h = H_ROUND; break;
+        case OP_ISFIN: u.h = H_ISFIN; break;
+        case OP_CASTBF: u.h = H_CASTBF; break;
+        default: u.h = H_HEAVY_U; break;   // log, rsqrt, recip
+      }
+      break;
+    default: u.h = H_BAD; break;
+  }
+  return u;
+}
+
+// does a word read FULL slot k?  (MOV from k, or a FULL binary operand in slot k)
+__device__ __forceinline__ bool reads_slot(const Instr& w, int k) {
+  if (w.op == OP_MOV) return !(w.flags & 1) && w.b == k;
+  if (w.op >= OP_ADD && w.op <= OP_POW) return !(w.flags & (CF_IMM | CF_XROW)) && w.a == k;
+  return false;
+}
+__device__ __forceinline__ bool writes_slot(const Instr& w, int k) {
+  if (w.op == OP_LD) return !(w.flags & LF_ROWV) && w.a == k;
+  if (w.op == OP_MOV) return !(w.flags & 1) && w.a == k;
+  return false;
+}
+// is FULL slot k read again after word i (before it is overwritten) within the section?
+__device__ __forceinline__ bool slot_live_after(const Instr* body, int n, int i, int k) {
+  for (int j = i + 1; j < n; j++) {
+    if (reads_slot(body[j], k)) return true;
+    if (writes_slot(body[j], k)) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ bool is_load_uop(uint8_t h) { return h >= H_LD_S4 && h <= H_LD_G; }
+__device__ __forceinline__ bool is_row_scalar(const Instr& w) {
+  if (w.op >= OP_ADD && w.op <= OP_POW) return (w.flags & CF_AROW) && (w.flags & (CF_XROW | CF_IMM));
+  if (w.op >= OP_SQRT && w.op <= OP_CASTBF) return (w.flags & CF_AROW) != 0;
+  return false;
+}
+
+// decode a section (thread 0; the caller synchronises the CTA before and after)
+__device__ __forceinline__ void decode_section(const Prog& P, const Instr* body, int n) {
+  if (threadIdx.x != 0) return;
+  Uop* U = uops();
+  int m = 0, hoisted = 0;
+  bool pend_wait = false;
+  for (int i = 0; i < n; i++) {
+    const Instr w = body[i];
+    if (w.op == OP_WAIT) {
+      pend_wait = true;
+      continue;
+    }
+    if (w.op == OP_REL) {
+      if (m > 0 && is_load_uop(U[m - 1].h) && (U[m - 1].fl & LF_DMA) && !(U[m - 1].fl & LF_HOIST)) {
+        U[m - 1].uf |= UF_REL;
+      } else {
+        Uop r = decode_word(P, body, i, hoisted);
+        U[m++] = r;
+      }
+      continue;
+    }
+    Uop u = decode_word(P, body, i, hoisted);
+    if (pend_wait) {
+      if (is_load_uop(u.h) && (u.fl & LF_DMA) && !(u.fl & LF_HOIST)) {
+        u.uf |= UF_WAIT;
+      } else {
+        Uop wt = u;
+        wt.h = H_WAIT;
+        wt.uf = 0;
+        wt.cnt = 0;
+        U[m++] = wt;
+      }
+      pend_wait = false;
+    }
+    if (is_load_uop(u.h) && w.a != 0) {
+      // REL words between this load and its consumer are folded first
+      int j = i + 1;
+      bool rel = false;
+      if (j < n && body[j].op == OP_REL && (u.fl & LF_DMA) && !(u.fl & LF_HOIST)) {
+        rel = true;
+        j++;
+      }
+      if (j < n) {
+        const Instr x = body[j];
+        if (x.op == OP_MOV && !(x.flags & 1) && x.a == 0 && x.b == w.a) {
+          // LD k <- t ; MOV 0 <- k
+          u.uf |= UF_TOACC;
+          if (!slot_live_after(body, n, j, w.a)) u.uf &= ~UF_STORE;
+          if (rel) u.uf |= UF_REL;
+          U[m++] = u;
+          i = j;
+          continue;
+        }
+        if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && x.a == w.a &&
+            !(x.flags & (CF_AROW | CF_XROW | CF_IMM))) {
+          // LD k <- t ; ACC <- ACC op k
+          u.uf |= UF_OP | ((x.flags & CF_REV) ? UF_REV : 0);
+          u.op = x.op;
+          if (!slot_live_after(body, n, j, w.a)) u.uf &= ~UF_STORE;
+          if (rel) u.uf |= UF_REL;
+          U[m++] = u;
+          i = j;
+          continue;
+        }
+      }
+    }
+    if (u.h == H_MOV_XA && i + 1 < n) {
+      // MOV k <- 0 ; ACC <- ACC op k  ==>  op with X = ACC, saving ACC to k first if k is read later
+      const Instr x = body[i + 1];
+      if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && x.a == w.a &&
+          !(x.flags & (CF_AROW | CF_XROW | CF_IMM))) {
+        Uop v = decode_word(P, body, i + 1, hoisted);
+        v.h = light_handler(x.op, 1, (x.flags & CF_REV) != 0);
+        if (slot_live_after(body, n, i + 1, w.a)) v.uf |= UF_SAVE;
+        U[m++] = v;
+        i++;
+        continue;
+      }
+    }
+    if (u.h == H_CASTBF && i + 1 < n && body[i + 1].op == OP_ST && !(body[i + 1].flags & LF_ROWV)) {
+      Uop v = decode_word(P, body, i + 1, hoisted);
+      v.uf |= UF_CAST;
+      U[m++] = v;
+      i++;
+      continue;
+    }
+    if ((u.h == H_RSUM_U || u.h == H_RMAX_U) && P.ur) {
+      // fold the ROW-scalar ops that follow (they act on this reduction's result)
+      U[m++] = u;
+      const int at = m - 1;
+      while (i + 1 < n && is_row_scalar(body[i + 1]) && U[at].cnt < 8) {
+        U[m++] = decode_word(P, body, i + 1, hoisted);
+        U[at].cnt++;
+        i++;
+      }
+      continue;
+    }
+    U[m++] = u;
+  }
+  if (pend_wait) {
+    Uop wt;
+    wt.h = H_WAIT;
+    wt.uf = 0;
+    wt.cnt = 0;
+    U[m++] = wt;
+  }
+  *uop_count() = m;
+}
+
+// ---- tile execution ----------------------------------------------------------------
+// row-value helpers: ROW values are the same in every lane of a warp, so every lane
+// writes the same numbers; the lanes finish reading old values before anyone writes,
+// and see the new ones only after all have written
+__device__ __forceinline__ void row_binary(int op, bool rev, float* dst, const float* xrow, float xi, int nv, int nvall) {
+  __syncwarp();
+  float r0 = 0.f;
+#pragma unroll 1
+  for (int v = 0; v < nv; v++) {
+    const float a = dst[v], x = xrow ? xrow[v] : xi;
+    const float r = rev ? bin_rt(op, x, a) : bin_rt(op, a, x);
+    if (v == 0) r0 = r;
+    __syncwarp();
+    dst[v] = r;
+    __syncwarp();
+  }
+  if (nv == 1) {
+    for (int v = 1; v < nvall; v++) dst[v] = r0;
+    __syncwarp();
+  }
+}
+__device__ __forceinline__ void row_unary(int op, float* dst, int nv, int nvall) {
+  __syncwarp();
+  float r0 = 0.f;
+#pragma unroll 1
+  for (int v = 0; v < nv; v++) {
+    const float r = unary_fn(op, dst[v]);
+    if (v == 0) r0 = r;
+    __syncwarp();
+    dst[v] = r;
+    __syncwarp();
+  }
+  if (nv == 1) {
+    for (int v = 1; v < nvall; v++) dst[v] = r0;
+    __syncwarp();
+  }
+}
+// the ROW-scalar micro-ops folded into a reduction, applied to its one-row result
+__device__ __forceinline__ float row_fold(const Uop* F, int cnt, float q, int warp) {
+#pragma unroll 1
+  for (int j = 0; j < cnt; j++) {
+    const Uop v = F[j];
+    if (v.h == H_ROWBIN) {
+      const float x = (v.fl & CF_XROW) ? rowslot(v.a, warp)[0] : v.imm;
+      q = (v.fl & CF_REV) ? bin_rt(v.op, x, q) : bin_rt(v.op, q, x);
+    } else {
+      q = unary_fn(v.op, q);
+    }
+  }
+  return q;
+}
+
 template <int VE>
-__device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P, const Instr* body, int n,
-                                          const TilePos& O, Lanes<VE>& L, int lane, int it, const Ctl& C,
-                                          float& grand, float (&A)[REG], int& rbuf, uint32_t tb) {
+__device__ __forceinline__ void ldg_full(float (&dst)[REG], const TensRec& T, const Prog& P, const Lanes<VE>& L,
+                                         const TilePos& O, const LaunchParams& Pm, uint32_t tb, bool full) {
+  const int dt = T.dtype;
+  const uint8_t* base = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
+  const int64_t vin = T.vs[P.r - 1];
+  const int esz = dtype_size(dt);
+  if (full && P.r <= 2 && vin == 1 && (((P.r == 2 ? T.vs[0] : 0) * esz) & 15) == 0) {
+    const int64_t vs0 = P.r == 2 ? T.vs[0] : 0;
+    if (dt == DT_F32) {
+      ldg_vectors_fast<VE, 4>(dst, base, vs0, O.oin, O, L);
+    } else if (dt == DT_BF16) {
+      if constexpr (VE >= 8) ldg_vectors_fast<VE, 2>(dst, base, vs0, O.oin, O, L);
+    } else {
+      if constexpr (VE == 16) ldg_vectors_fast<VE, 1>(dst, base, vs0, O.oin, O, L);
+    }
+    return;
+  }
+  // general masked path (ragged tails, strided views, rank > 2): a rolled loop through
+  // the TMEM scratch register keeps it compact
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+#pragma unroll 1
+  for (int j = 0; j < REG; j++) {
+    const int v = j / VE, e = j % VE;
+    const int s = warp * P.nvu + v;
+    const int row = s / P.m, col = (s % P.m) * (VE * 32) + lane * VE;
+    float x = 0.f;
+    int64_t off;
+    if (v < P.nvu && s < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
+      x = load_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt);
+    tm_st1(tm_scratch(tb) + (uint32_t)j, x);
+  }
+  tm_ld32(tm_scratch(tb), dst);
+}
+
+template <int VE>
+__device__ __forceinline__ void st_full(const float (&acc)[REG], const TensRec& T, const Prog& P, const Lanes<VE>& L,
+                                        const TilePos& O, const LaunchParams& Pm, uint32_t tb, bool full) {
+  const int dt = T.dtype;
+  const int esz = dtype_size(dt);
+  uint8_t* base = static_cast<uint8_t*>(Pm.ptrs[T.binding]);
+  const int64_t vin = T.vs[P.r - 1];
+  if (full && P.r <= 2 && vin == 1 && (((P.r == 2 ? T.vs[0] : 0) * esz) & 15) == 0) {
+    const int64_t vs0 = P.r == 2 ? T.vs[0] : 0;
+    if (dt == DT_F32) {
+      stg_vectors_fast<VE, 4>(acc, base, vs0, O.oin, O, L);
+    } else if (dt == DT_BF16) {
+      if constexpr (VE >= 8) stg_vectors_fast<VE, 2>(acc, base, vs0, O.oin, O, L);
+    } else {
+      if constexpr (VE == 16) stg_vectors_fast<VE, 1>(acc, base, vs0, O.oin, O, L);
+    }
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  tm_st32(tm_scratch(tb), acc);
+#pragma unroll 1
+  for (int j = 0; j < REG; j++) {
+    const int v = j / VE, e = j % VE;
+    const int s = warp * P.nvu + v;
+    const int row = s / P.m, col = (s % P.m) * (VE * 32) + lane * VE;
+    const float x = tm_ld1(tm_scratch(tb) + (uint32_t)j);
+    int64_t off;
+    if (v < P.nvu && s < P.segs && row_off(P, O, row, T.vs, off) && O.oin + col + e < P.n_in)
+      store_scalar(base, off + (int64_t)(O.oin + col + e) * vin, dt, x);
+  }
+}
+
+// one unrolled register loop of a unary function
+#define DVM_MAP(EXPR)                                          \
+  _Pragma("unroll") for (int e = 0; e < REG; e++) {            \
+    const float x = A[e];                                      \
+    A[e] = (EXPR);                                             \
+  }
+
+template <int VE>
+__device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P, const TilePos& O, Lanes<VE>& L,
+                                          int lane, int it, const Ctl& C, float& grand, float (&A)[REG], int& rbuf,
+                                          uint32_t tb, uint32_t& hmask) {
   constexpr int NV = REG / VE;
   const int warp = threadIdx.x >> 5;
   float* Q0 = rowslot(0, warp);   // ROW value of ACC (per vector)
   const int nvr = P.ur ? 1 : NV;  // ROW values that differ within a thread
   lanes_for_tile<VE>(P, O, L);
+  // the tile is complete for this warp: every vector inside, no ragged inner tail
+  const bool full = L.rowok == L.seg && O.oin + P.t_in <= P.n_in;
   const int stage = C.n_stages ? it % C.n_stages : 0;
   const uint32_t parity = C.n_stages ? (uint32_t)((it / C.n_stages) & 1) : 0;
   const uint8_t* stage_base = dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes;
+  const Uop* U = uops();
+  const int n = *uop_count();
   for (int pc = 0; pc < n; pc++) {
-    const Instr w = body[pc];
-    const uint8_t fl = w.flags;
-    switch (w.op) {
-      case OP_WAIT:
+    const Uop u = U[pc];
+    float X[REG];
+    switch (u.h) {
+      case H_NOP:
+        break;
+      case H_WAIT:
         mbar_wait(bar_full(stage), parity, C.st, abort_flag());
         break;
-      case OP_REL:
+      case H_REL:
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty(stage));
         break;
-      case OP_LD:
-        if (fl & LF_ROWV) {
-          // one value per tile row from a [.., 1]-shaped tensor
-          const TensRec& Tn = P.tens[w.b];
-          const uint8_t* base = static_cast<const uint8_t*>(Pm.ptrs[Tn.binding]);
-          float* dst = rowslot(w.a, warp);
-          __syncwarp();
-#pragma unroll 1
-          for (int v = 0; v < nvr; v++) {
-            float q = 0.f;
-            int64_t off;
-            if (((L.rowok >> v) & 1u) && row_off(P, O, L.row(v), Tn.vs, off)) q = load_scalar(base, off, Tn.dtype);
-            dst[v] = q;
-          }
-          if (P.ur) row_fill(dst, NV);
-          __syncwarp();
-        } else if (w.a == 0) {
-          op_load<VE>(A, w, P, L, O, Pm, stage_base, tb);
+      // -------------------------------------------------------------- loads
+      case H_LD_S4:
+      case H_LD_S2:
+      case H_LD_S1:
+      case H_LD_H:
+      case H_LD_G: {
+        if (u.uf & UF_WAIT) mbar_wait(bar_full(stage), parity, C.st, abort_flag());
+        if (u.h == H_LD_G) {
+          ldg_full<VE>(X, P.tens[u.b], P, L, O, Pm, tb, full);
         } else {
-          float X[REG];
-          op_load<VE>(X, w, P, L, O, Pm, stage_base, tb);
-          tm_st32(tm_slot(tb, w.a), X);
-        }
-        break;
-      case OP_ST:
-        if (fl & LF_ROWV) {
-          // the row's first segment (lane 0) writes it
-          const TensRec& Tn = P.tens[w.a];
-          uint8_t* base = static_cast<uint8_t*>(Pm.ptrs[Tn.binding]);
-#pragma unroll 1
-          for (int v = 0; v < NV; v++) {
-            const int s = warp * P.nvu + v;
-            int64_t off;
-            if (lane == 0 && ((L.rowok >> v) & 1u) && s % P.m == 0 && row_off(P, O, L.row(v), Tn.vs, off))
-              store_scalar(base, off, Tn.dtype, Q0[v]);
-          }
-        } else {
-          op_store<VE>(A, w, P, L, O, Pm, tb);
-        }
-        break;
-      case OP_MOV:
-        if (fl & 1) {  // ROW value: copy between per-warp ROW areas
-          const float* src = rowslot(w.b, warp);
-          float* dst = rowslot(w.a, warp);
-          __syncwarp();
-          float t[NV];
-#pragma unroll
-          for (int v = 0; v < NV; v++) t[v] = src[v];
-          __syncwarp();
-#pragma unroll
-          for (int v = 0; v < NV; v++) dst[v] = t[v];
-          __syncwarp();
-        } else if (w.a == 0) {
-          if (w.b != 0) tm_ld32(tm_slot(tb, w.b), A);
-        } else if (w.b == 0) {
-          tm_st32(tm_slot(tb, w.a), A);
-        } else {
-          float X[REG];
-          tm_ld32(tm_slot(tb, w.b), X);
-          tm_st32(tm_slot(tb, w.a), X);
-        }
-        break;
-      case OP_BCAST:
-        bcast_row<VE>(A, Q0);
-        break;
-      case OP_ADD: case OP_SUB: case OP_MUL: case OP_DIV: case OP_MAX: case OP_MIN: case OP_POW: {
-        const bool rev = fl & CF_REV;
-        const bool ar = fl & CF_AROW, xr = fl & CF_XROW, imm = fl & CF_IMM;
-        const float xi = __uint_as_float(w.imm);
-        if (ar && (xr || imm)) {
-          // ROW op ROW -> ROW
-          row_binary(w.op, rev, Q0, xr ? rowslot(w.a, warp) : nullptr, xi, nvr);
-          if (P.ur) row_fill(Q0, NV);
-          break;
-        }
-        if (w.op == OP_DIV || w.op == OP_POW) {
-          // FULL result through the scratch register
-          if (ar) bcast_row<VE>(A, Q0);
-          uint32_t xcol = 0;
-          if (!xr && !imm) {
-            if (w.a == 0) {
-              tm_st32(tm_slot(tb, 1) + 96u, A);  // X = ACC itself: a copy next to the scratch
-              xcol = tm_slot(tb, 1) + 96u;
+          const int rs = (u.fl & LF_COLV) ? 0 : P.t_in;
+          const uint8_t* region = ((u.fl & LF_HOIST) ? dvm_smem : stage_base) + u.off;
+          const int k = u.aux >> 4;
+          if (u.h == H_LD_H && (hmask & (1u << k))) {
+            tm_ld32(tm_hoist(tb, k), X);
+          } else {
+            const int esz = u.h == H_LD_S4 ? 4 : u.h == H_LD_S2 ? 2 : u.h == H_LD_S1 ? 1 : (u.aux & 15);
+            if (esz == 4) {
+              lds_vectors<VE, 4>(X, region, rs, L);
+            } else if (esz == 2) {
+              if constexpr (VE >= 8) lds_vectors<VE, 2>(X, region, rs, L);
             } else {
-              xcol = tm_slot(tb, w.a);
+              if constexpr (VE == 16) lds_vectors<VE, 1>(X, region, rs, L);
+            }
+            if (u.h == H_LD_H) {
+              tm_st32(tm_hoist(tb, k), X);
+              hmask |= 1u << k;
             }
           }
-          tm_st32(tm_scratch(tb), A);
-          heavy_binary_loop(w.op, rev, tm_scratch(tb), !xr && !imm, xcol, xr ? rowslot(w.a, warp) : nullptr, xi, VE);
-          tm_ld32(tm_scratch(tb), A);
-          break;
         }
-        // light ops: the operand is an immediate, a ROW area, ACC, or a slot from TMEM
+        if (u.uf & UF_REL) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty(stage));
+        }
+        if (u.uf & UF_STORE) tm_st32(tm_slot(tb, u.a), X);
+        if (u.uf & UF_OP) {
+          if (u.op == OP_ADD) bin_ff_<OP_ADD, false>(A, X);
+          else if (u.op == OP_MUL) bin_ff_<OP_MUL, false>(A, X);
+          else if (u.uf & UF_REV) bin_ff_<OP_SUB, true>(A, X);
+          else bin_ff_<OP_SUB, false>(A, X);
+        } else if (u.uf & UF_TOACC) {
+#pragma unroll
+          for (int e = 0; e < REG; e++) A[e] = X[e];
+        }
+        break;
+      }
+      case H_LDROW: {
+        // one value per tile row from a [.., 1]-shaped tensor
+        const TensRec& Tn = P.tens[u.b];
+        const uint8_t* base = static_cast<const uint8_t*>(Pm.ptrs[Tn.binding]);
+        float* dst = rowslot(u.a, warp);
+        __syncwarp();
+        float q0 = 0.f;
+#pragma unroll 1
+        for (int v = 0; v < nvr; v++) {
+          float q = 0.f;
+          int64_t off;
+          if (((L.rowok >> v) & 1u) && row_off(P, O, L.row(v), Tn.vs, off)) q = load_scalar(base, off, Tn.dtype);
+          if (v == 0) q0 = q;
+          dst[v] = q;
+        }
+        if (P.ur)
+          for (int v = 1; v < NV; v++) dst[v] = q0;
+        __syncwarp();
+        break;
+      }
+      // -------------------------------------------------------------- stores
+      case H_ST:
+        if (u.uf & UF_CAST) DVM_MAP(round_bf16(x))
+        st_full<VE>(A, P.tens[u.a], P, L, O, Pm, tb, full);
+        break;
+      case H_STROW: {
+        // the row's first segment (lane 0) writes it
+        const TensRec& Tn = P.tens[u.a];
+        uint8_t* base = static_cast<uint8_t*>(Pm.ptrs[Tn.binding]);
+#pragma unroll 1
+        for (int v = 0; v < NV; v++) {
+          const int s = warp * P.nvu + v;
+          int64_t off;
+          if (lane == 0 && ((L.rowok >> v) & 1u) && s % P.m == 0 && row_off(P, O, L.row(v), Tn.vs, off))
+            store_scalar(base, off, Tn.dtype, Q0[v]);
+        }
+        break;
+      }
+      // -------------------------------------------------------------- moves
+      case H_MOV_AX:
+        tm_ld32(tm_slot(tb, u.b), A);
+        break;
+      case H_MOV_XA:
+        tm_st32(tm_slot(tb, u.a), A);
+        break;
+      case H_MOV_XX:
+        tm_ld32(tm_slot(tb, u.b), X);
+        tm_st32(tm_slot(tb, u.a), X);
+        break;
+      case H_MOVROW: {
+        const float* src = rowslot(u.b, warp);
+        float* dst = rowslot(u.a, warp);
+        __syncwarp();
+        float t[NV];
+#pragma unroll
+        for (int v = 0; v < NV; v++) t[v] = src[v];
+        __syncwarp();
+#pragma unroll
+        for (int v = 0; v < NV; v++) dst[v] = t[v];
+        __syncwarp();
+        break;
+      }
+      case H_BCAST:
+        bcast_row<VE>(A, Q0);
+        break;
+      // -------------------------------------------------------------- light binary
+#define DVM_LIGHT(HT, HI, HR, OPC, REV)                                          \
+      case HT:                                                                   \
+        tm_ld32(tm_slot(tb, u.a), X);                                            \
+        bin_ff_<OPC, REV>(A, X);                                                 \
+        break;                                                                   \
+      case HI: {                                                                 \
+        float xv[NV];                                                            \
+        _Pragma("unroll") for (int v = 0; v < NV; v++) xv[v] = u.imm;           \
+        bin_fv_<VE, OPC, REV>(A, xv);                                            \
+        break;                                                                   \
+      }                                                                          \
+      case HR: {                                                                 \
+        float xv[NV];                                                            \
+        const float* xrow = rowslot(u.a, warp);                                  \
+        _Pragma("unroll") for (int v = 0; v < NV; v++) xv[v] = xrow[v];          \
+        bin_fv_<VE, OPC, REV>(A, xv);                                            \
+        break;                                                                   \
+      }
+      DVM_LIGHT(H_ADD_T, H_ADD_I, H_ADD_R, OP_ADD, false)
+      DVM_LIGHT(H_SUB_T, H_SUB_I, H_SUB_R, OP_SUB, false)
+      DVM_LIGHT(H_RSUB_T, H_RSUB_I, H_RSUB_R, OP_SUB, true)
+      DVM_LIGHT(H_MUL_T, H_MUL_I, H_MUL_R, OP_MUL, false)
+#undef DVM_LIGHT
+      case H_ADD_A:
+        if (u.uf & UF_SAVE) tm_st32(tm_slot(tb, u.a), A);
+#pragma unroll
+        for (int e = 0; e < REG; e++) X[e] = A[e];
+        bin_ff_<OP_ADD, false>(A, X);
+        break;
+      case H_SUB_A:
+        if (u.uf & UF_SAVE) tm_st32(tm_slot(tb, u.a), A);
+#pragma unroll
+        for (int e = 0; e < REG; e++) A[e] = A[e] - A[e];
+        break;
+      case H_MUL_A:
+        if (u.uf & UF_SAVE) tm_st32(tm_slot(tb, u.a), A);
+#pragma unroll
+        for (int e = 0; e < REG; e++) X[e] = A[e];
+        bin_ff_<OP_MUL, false>(A, X);
+        break;
+#define DVM_VLIGHT(H, OPC, REV)                                                  \
+      case H: {                                                                  \
+        tm_ld32(tm_slot(tb, u.a), X);                                            \
+        float av[NV];                                                            \
+        _Pragma("unroll") for (int v = 0; v < NV; v++) av[v] = Q0[v];            \
+        bin_vf_<VE, OPC, REV>(A, av, X);                                         \
+        break;                                                                   \
+      }
+      DVM_VLIGHT(H_VADD_T, OP_ADD, false)
+      DVM_VLIGHT(H_VSUB_T, OP_SUB, false)
+      DVM_VLIGHT(H_VRSUB_T, OP_SUB, true)
+      DVM_VLIGHT(H_VMUL_T, OP_MUL, false)
+#undef DVM_VLIGHT
+      case H_BIN_GEN: {
+        // MAX / MIN and rare forms: operand kinds resolved at run time
+        const bool rev = u.fl & CF_REV;
+        const bool ar = u.fl & CF_AROW, xr = u.fl & CF_XROW, imm = u.fl & CF_IMM;
         if (imm || xr) {
           float xv[NV];
-          const float* xrow = rowslot(w.a, warp);
+          const float* xrow = rowslot(u.a, warp);
 #pragma unroll
-          for (int v = 0; v < NV; v++) xv[v] = imm ? xi : xrow[v];
-          switch (w.op) {
+          for (int v = 0; v < NV; v++) xv[v] = imm ? u.imm : xrow[v];
+          switch (u.op) {
             case OP_ADD: bin_fv<VE, OP_ADD>(A, xv, rev); break;
             case OP_SUB: bin_fv<VE, OP_SUB>(A, xv, rev); break;
             case OP_MUL: bin_fv<VE, OP_MUL>(A, xv, rev); break;
@@ -1041,18 +1457,17 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
           }
           break;
         }
-        float X[REG];
-        if (w.a == 0) {
+        if (u.a == 0) {
 #pragma unroll
           for (int e = 0; e < REG; e++) X[e] = A[e];
         } else {
-          tm_ld32(tm_slot(tb, w.a), X);
+          tm_ld32(tm_slot(tb, u.a), X);
         }
         if (ar) {
           float av[NV];
 #pragma unroll
           for (int v = 0; v < NV; v++) av[v] = Q0[v];
-          switch (w.op) {
+          switch (u.op) {
             case OP_ADD: bin_vf<VE, OP_ADD>(A, av, X, rev); break;
             case OP_SUB: bin_vf<VE, OP_SUB>(A, av, X, rev); break;
             case OP_MUL: bin_vf<VE, OP_MUL>(A, av, X, rev); break;
@@ -1060,7 +1475,7 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
             default: bin_vf<VE, OP_MIN>(A, av, X, rev); break;
           }
         } else {
-          switch (w.op) {
+          switch (u.op) {
             case OP_ADD: bin_ff<OP_ADD>(A, X, rev); break;
             case OP_SUB: bin_ff<OP_SUB>(A, X, rev); break;
             case OP_MUL: bin_ff<OP_MUL>(A, X, rev); break;
@@ -1070,127 +1485,172 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         }
         break;
       }
-      case OP_RSUM:
-      case OP_RMAX: {
-        // ACC (FULL) -> ACC (ROW).  Fixed order: each thread combines its vectors of one
-        // row in order, the warp butterfly combines the lanes, then every thread of the
-        // row adds the warps' (or segments') partials in order.
-        const bool mx = w.op == OP_RMAX;
+      // -------------------------------------------------------------- ROW ops
+      case H_ROWBIN:
+        row_binary((int)u.op, (u.fl & CF_REV) != 0, Q0, (u.fl & CF_XROW) ? rowslot(u.a, warp) : nullptr, u.imm, nvr,
+                   NV);
+        break;
+      case H_ROWUN:
+        row_unary((int)u.op, Q0, nvr, NV);
+        break;
+      // -------------------------------------------------------------- heavy
+      case H_DIVPOW: {
+        // FULL result through the scratch register
+        const bool rev = u.fl & CF_REV;
+        const bool ar = u.fl & CF_AROW, xr = u.fl & CF_XROW, imm = u.fl & CF_IMM;
+        if (ar) bcast_row<VE>(A, Q0);
+        uint32_t xcol = 0;
+        if (!xr && !imm) {
+          if (u.a == 0) {
+            tm_st32(tm_spare(tb), A);  // X = ACC itself: a copy in the spare register
+            xcol = tm_spare(tb);
+          } else {
+            xcol = tm_slot(tb, u.a);
+          }
+        }
+        tm_st32(tm_scratch(tb), A);
+        heavy_binary_loop((int)u.op, rev, tm_scratch(tb), !xr && !imm, xcol, xr ? rowslot(u.a, warp) : nullptr,
+                          u.imm, VE);
+        tm_ld32(tm_scratch(tb), A);
+        break;
+      }
+      case H_SQRT:
+        DVM_MAP(sqrtf(x))
+        break;
+      case H_EXP:
+        DVM_MAP(expf(x))
+        break;
+      case H_SILU:
+        DVM_MAP(x / (1.0f + expf(-x)))
+        break;
+      case H_HEAVY_U:
+        tm_st32(tm_scratch(tb), A);
+        heavy_unary_loop((int)u.op, tm_scratch(tb));
+        tm_ld32(tm_scratch(tb), A);
+        break;
+      // -------------------------------------------------------------- light unary
+      case H_ABS:
+        DVM_MAP(fabsf(x))
+        break;
+      case H_NEG:
+        DVM_MAP(-x)
+        break;
+      case H_FLOOR:
+        DVM_MAP(floorf(x))
+        break;
+      case H_ROUND:
+        DVM_MAP(rintf(x))
+        break;
+      case H_ISFIN:
+        DVM_MAP(isfinite(x) ? 1.f : 0.f)
+        break;
+      case H_CASTBF:
+        DVM_MAP(round_bf16(x))
+        break;
+      // -------------------------------------------------------------- reductions
+      case H_RSUM_U:
+      case H_RMAX_U: {
+        // ACC (FULL) -> ACC (ROW), one tile row per thread.  Fixed order: the thread's
+        // vectors in order (two interleaved partial sums), the warp butterfly, then
+        // the partials of the row's warps in warp order; then the folded ROW ops.
+        const bool mx = u.h == H_RMAX_U;
         const float ident = mx ? -INFINITY : 0.f;
         float* red = red_buf(rbuf);
         rbuf ^= 1;
-        if (P.ur) {
-          float p = ident;
+        float s0 = ident, s1 = ident;
+        if (full) {
 #pragma unroll
           for (int v = 0; v < NV; v++) {
             if (!((L.seg >> v) & 1u)) continue;
-            if ((L.rowok >> v) & 1u) {
-              const int nc = ncol<VE>(P, O, L, v);
-              float s0 = ident, s1 = ident;
-              if (nc == VE) {
 #pragma unroll
-                for (int e = 0; e < VE; e += 2) {
-                  s0 = mx ? vmax(s0, A[v * VE + e]) : s0 + A[v * VE + e];
-                  s1 = mx ? vmax(s1, A[v * VE + e + 1]) : s1 + A[v * VE + e + 1];
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < VE; e++)
-                  if (e < nc) s0 = mx ? vmax(s0, A[v * VE + e]) : s0 + A[v * VE + e];
-              }
-              const float s = mx ? vmax(s0, s1) : s0 + s1;
-              p = mx ? vmax(p, s) : p + s;
+            for (int e = 0; e < VE; e += 2) {
+              s0 = mx ? vmax(s0, A[v * VE + e]) : s0 + A[v * VE + e];
+              s1 = mx ? vmax(s1, A[v * VE + e + 1]) : s1 + A[v * VE + e + 1];
             }
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < NV; v++) {
+            if (!((L.rowok >> v) & 1u)) continue;
+            const int nc = ncol<VE>(P, O, L, v);
+#pragma unroll
+            for (int e = 0; e < VE; e++)
+              if (e < nc) s0 = mx ? vmax(s0, A[v * VE + e]) : s0 + A[v * VE + e];
+          }
+        }
+        float p = mx ? vmax(s0, s1) : s0 + s1;
+        p = mx ? warp_reduce<true>(p) : warp_reduce<false>(p);
+        if (lane == 0 && L.seg) red[warp] = p;
+        consumer_sync();
+        float q = ident;
+        if (L.seg)
+          for (int k = L.rw0; k < L.rw1; k++) q = mx ? vmax(q, red[k]) : q + red[k];
+        if (u.cnt) q = row_fold(U + pc + 1, u.cnt, q, warp);
+        __syncwarp();
+#pragma unroll
+        for (int v = 0; v < NV; v++) Q0[v] = q;
+        __syncwarp();
+        pc += u.cnt;
+        break;
+      }
+      case H_RRED_G: {
+        // general: one butterfly per segment, then each row's segments in order
+        const bool mx = u.op == OP_RMAX;
+        const float ident = mx ? -INFINITY : 0.f;
+        float* red = red_buf(rbuf);
+        rbuf ^= 1;
+#pragma unroll
+        for (int v = 0; v < NV; v++) {
+          if (!((L.seg >> v) & 1u)) continue;   // warp-uniform
+          float p = ident;
+          if ((L.rowok >> v) & 1u) {
+            const int nc = ncol<VE>(P, O, L, v);
+#pragma unroll
+            for (int e = 0; e < VE; e++)
+              if (e < nc) p = mx ? vmax(p, A[v * VE + e]) : p + A[v * VE + e];
           }
           p = mx ? warp_reduce<true>(p) : warp_reduce<false>(p);
-          if (lane == 0 && L.seg) red[warp] = p;
-          consumer_sync();
+          if (lane == 0) red[warp * P.nvu + v] = p;
+        }
+        consumer_sync();
+        __syncwarp();
+#pragma unroll 1
+        for (int v = 0; v < NV; v++) {
           float q = ident;
-          if (L.seg)
-            for (int k = L.rw0; k < L.rw1; k++) q = mx ? vmax(q, red[k]) : q + red[k];
-          __syncwarp();
-#pragma unroll
-          for (int v = 0; v < NV; v++) Q0[v] = q;
-          __syncwarp();
-        } else {
-          // general: one butterfly per segment, then each row's segments in order
-#pragma unroll
-          for (int v = 0; v < NV; v++) {
-            if (!((L.seg >> v) & 1u)) continue;   // warp-uniform
-            float p = ident;
-            if ((L.rowok >> v) & 1u) {
-              const int nc = ncol<VE>(P, O, L, v);
-#pragma unroll
-              for (int e = 0; e < VE; e++)
-                if (e < nc) p = mx ? vmax(p, A[v * VE + e]) : p + A[v * VE + e];
-            }
-            p = mx ? warp_reduce<true>(p) : warp_reduce<false>(p);
-            if (lane == 0) red[warp * P.nvu + v] = p;
+          if ((L.seg >> v) & 1u) {
+            const int s0 = L.row(v) * P.m;
+            for (int k = 0; k < P.m; k++) q = mx ? vmax(q, red[s0 + k]) : q + red[s0 + k];
           }
-          consumer_sync();
-          __syncwarp();
-#pragma unroll 1
-          for (int v = 0; v < NV; v++) {
-            float q = ident;
-            if ((L.seg >> v) & 1u) {
-              const int s0 = L.row(v) * P.m;
-              for (int k = 0; k < P.m; k++) q = mx ? vmax(q, red[s0 + k]) : q + red[s0 + k];
-            }
-            Q0[v] = q;
-          }
-          __syncwarp();
+          Q0[v] = q;
         }
+        __syncwarp();
         break;
       }
-      case OP_ASUM:
-        if (fl & CF_AROW) {
-          // one value per row: the thread holding the row's first segment (lane 0)
+      case H_ASUM:
+#pragma unroll
+        for (int v = 0; v < NV; v++)
+          if ((L.rowok >> v) & 1u) {
+            const int nc = ncol<VE>(P, O, L, v);
+#pragma unroll
+            for (int e = 0; e < VE; e++)
+              if (e < nc) grand += A[v * VE + e];
+          }
+        break;
+      case H_ASUM_ROW:
+        // one value per row: the thread holding the row's first segment (lane 0)
 #pragma unroll 1
-          for (int v = 0; v < NV; v++) {
-            const int s = warp * P.nvu + v;
-            if (lane == 0 && ((L.rowok >> v) & 1u) && s % P.m == 0) grand += Q0[v];
-          }
-        } else {
-#pragma unroll
-          for (int v = 0; v < NV; v++)
-            if ((L.rowok >> v) & 1u) {
-              const int nc = ncol<VE>(P, O, L, v);
-#pragma unroll
-              for (int e = 0; e < VE; e++)
-                if (e < nc) grand += A[v * VE + e];
-            }
+        for (int v = 0; v < NV; v++) {
+          const int s = warp * P.nvu + v;
+          if (lane == 0 && ((L.rowok >> v) & 1u) && s % P.m == 0) grand += Q0[v];
         }
         break;
-      case OP_SQRT: case OP_ABS: case OP_LOG: case OP_EXP: case OP_ROUND: case OP_FLOOR:
-      case OP_ISFIN: case OP_NEG: case OP_RSQRT: case OP_RECIP: case OP_SILU: case OP_CASTBF: {
-        const int op = w.op;
-        if (fl & CF_AROW) {
-          row_unary(op, Q0, nvr);
-          if (P.ur) row_fill(Q0, NV);
-        } else if (heavy_unary(op)) {
-          tm_st32(tm_scratch(tb), A);
-          heavy_unary_loop(op, tm_scratch(tb));
-          tm_ld32(tm_scratch(tb), A);
-        } else {
-          switch (op) {  // light ops: one unrolled register loop per opcode
-#define DVM_UNARY_CASE(OPC)                                                        \
-  case OPC:                                                                        \
-    _Pragma("unroll") for (int e = 0; e < REG; e++) A[e] = unary_fn(OPC, A[e]);    \
-    break;
-            DVM_UNARY_CASE(OP_ABS) DVM_UNARY_CASE(OP_ROUND) DVM_UNARY_CASE(OP_FLOOR) DVM_UNARY_CASE(OP_ISFIN)
-            DVM_UNARY_CASE(OP_NEG) DVM_UNARY_CASE(OP_CASTBF)
-#undef DVM_UNARY_CASE
-            default: break;
-          }
-        }
-        break;
-      }
       default:
         set_status(Pm.status, -101 /* DVM_E_BAD_OPCODE */);
         break;
     }
   }
 }
+#undef DVM_MAP
 
 // ---- grid-wide sum (GSUM) -------------------------------------------------
 // Called by every thread of the CTA.  The result is
@@ -1240,63 +1700,91 @@ __device__ __forceinline__ float grid_sum(const LaunchParams& Pm, float grand, i
 __device__ __forceinline__ void issue_upto(const LaunchParams& Pm, const uint8_t* img, const Ctl& C, int a, int need,
                                            int limit, bool plain) {
   Issuer& I = issuer();
-  while (I.issued < limit && !*abort_flag()) {
+  // the hot state in registers for the whole call, written back at the end
+  int issued = I.issued, g = I.g, tau = I.tau, c0 = I.c0, cin = I.cin;
+  const int g_end = I.g_end, t_end = I.t_end;
+  int prog = I.prog, stage_sec = I.stage_sec, r = I.r, t0 = I.t0, t_in = I.t_in, tiles_in = I.tiles_in;
+  int end = 0;
+  if (plain) {
+    const ProgRec* pr = reinterpret_cast<const ProgRec*>(img + sizeof(Header) + prog * sizeof(ProgRec));
+    end = (int)(pr->tile_base + pr->block_dim);
+  }
+  while (issued < limit && !*abort_flag()) {
     if (plain) {
-      while (true) {
-        if (I.g >= I.g_end) return;
-        const ProgRec* pr = reinterpret_cast<const ProgRec*>(img + sizeof(Header) + I.prog * sizeof(ProgRec));
-        const int end = (int)(pr->tile_base + pr->block_dim);
-        if (I.g >= end) {  // the current program is done: set up the next one
-          I.prog++;
-          Prog Q;
-          load_prog(img, I.prog, Q, a);
-          dma_section(I, Q, Pm, Q.body + 1, (int)Q.body[0].imm);
-          I.tau = I.g - (int)Q.pr->tile_base;
-          I.c0 = I.tau / Q.tiles_in;
-          I.cin = I.tau - I.c0 * Q.tiles_in;
-          continue;
+      if (g >= g_end) break;
+      if (g >= end || !stage_sec) {
+        bool more = true;
+        while (true) {
+          if (g >= g_end) {
+            more = false;
+            break;
+          }
+          if (g >= end) {  // the current program is done: set up the next one
+            prog++;
+            Prog Q;
+            load_prog(img, prog, Q, a);
+            dma_section(I, Q, Pm, Q.body + 1, (int)Q.body[0].imm);
+            end = (int)(Q.pr->tile_base + Q.pr->block_dim);
+            tau = g - (int)Q.pr->tile_base;
+            c0 = tau / Q.tiles_in;
+            cin = tau - c0 * Q.tiles_in;
+            stage_sec = I.stage_sec;
+            r = Q.r;
+            t0 = Q.t0;
+            t_in = Q.t_in;
+            tiles_in = Q.tiles_in;
+            continue;
+          }
+          if (!stage_sec) {  // nothing to stage in this program: skip its tiles
+            g = end;
+            continue;
+          }
+          break;
         }
-        if (!I.stage_sec) {  // nothing to stage in this program: skip its tiles
-          I.g = end;
-          continue;
-        }
-        break;
+        if (!more) break;
       }
-    } else if (I.tau >= I.t_end || !I.stage_sec) {
-      return;
+    } else if (tau >= t_end || !stage_sec) {
+      break;
     }
-    const int stage = I.issued % C.n_stages;
-    const uint32_t parity = ((I.issued / C.n_stages) & 1) ^ 1;
-    if (I.issued >= need) {
-      if (!mbar_try_wait(bar_empty(stage), parity)) return;  // not free yet: try again next tile
+    const int stage = issued % C.n_stages;
+    const uint32_t parity = ((issued / C.n_stages) & 1) ^ 1;
+    if (issued >= need) {
+      if (!mbar_try_wait(bar_empty(stage), parity)) break;  // not free yet: try again next tile
     } else if (!mbar_wait(bar_empty(stage), parity, C.st, abort_flag())) {
-      return;
+      break;
     }
-    // tile origin from the cached geometry (rank <= 2 incrementally, else by division)
+    // tile origin (rank <= 2 incrementally, else by division)
     int od[3] = {0, 0, 0};
     int oin;
-    if (I.r <= 2) {
-      od[0] = I.r == 2 ? I.c0 * I.t0 : 0;
-      oin = I.cin * I.t_in;
+    if (r <= 2) {
+      od[0] = r == 2 ? c0 * t0 : 0;
+      oin = cin * t_in;
     } else {
-      int tau = I.tau;
-      oin = (tau % I.tiles_in) * I.t_in;
-      tau /= I.tiles_in;
-      for (int dd = I.r - 2; dd >= 0; dd--) {
-        const int td = (int)((I.pr->n[dd] + I.pr->t[dd] - 1) / I.pr->t[dd]);
-        od[dd] = (tau % td) * (int)I.pr->t[dd];
-        tau /= td;
+      const ProgRec* pr = I.pr;
+      int tt = tau;
+      oin = (tt % tiles_in) * t_in;
+      tt /= tiles_in;
+      for (int dd = r - 2; dd >= 0; dd--) {
+        const int td = (int)((pr->n[dd] + pr->t[dd] - 1) / pr->t[dd]);
+        od[dd] = (tt % td) * (int)pr->t[dd];
+        tt /= td;
       }
     }
     issue_tile(I, od[0], od[1], od[2], oin, dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes, bar_full(stage));
-    I.issued++;
-    I.tau++;
-    if (++I.cin == I.tiles_in) {
-      I.cin = 0;
-      I.c0++;
+    issued++;
+    tau++;
+    if (++cin == tiles_in) {
+      cin = 0;
+      c0++;
     }
-    if (plain) I.g++;
+    if (plain) g++;
   }
+  I.issued = issued;
+  I.g = g;
+  I.tau = tau;
+  I.c0 = c0;
+  I.cin = cin;
+  I.prog = prog;
 }
 
 // ---- the kernel --------------------------------------------------------------
@@ -1371,6 +1859,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
   for (int e = 0; e < REG; e++) A[e] = 0.f;
   float grand = 0.f;
   int rbuf = 0;
+  uint32_t hmask = 0;   // hoisted-load cache registers filled for the current section
   int it = 0;  // staged tiles consumed
   Lanes<VE> L;
   Prog P;
@@ -1388,7 +1877,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
     p = 0;
     load_prog(smem, 0, P, a);
     lanes_for_prog<VE>(P, warp, lane, L);
+    __syncthreads();
     fill_tables<VE>(P);
+    __syncthreads();
   }
   while (true) {
     if (!sectioned) {
@@ -1400,9 +1891,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
           p++;
         load_prog(smem, p, P, a);
         lanes_for_prog<VE>(P, warp, lane, L);
-        fill_tables<VE>(P);
         sec = P.body + 1;
         sec_n = (int)P.body[0].imm;
+        __syncthreads();  // the previous program's tiles may still read the tables
+        fill_tables<VE>(P);
+        decode_section(P, sec, sec_n);
+        hmask = 0;
+        __syncthreads();
         staged = section_has_stage(sec, sec_n);
         tau = g - (int)P.pr->tile_base;
         pos_start(P, T, tau);
@@ -1433,6 +1928,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
           tau = lo;
           t_end = min(hi, (int)P.pr->block_dim);
           pc += 1 + sec_n;
+          __syncthreads();  // the previous section's tiles may still read the micro-ops
+          decode_section(P, sec, sec_n);
+          hmask = 0;
+          __syncthreads();
           if (tau < t_end) {
             pos_start(P, T, tau);
             if (tid == 0 && staged) {
@@ -1471,7 +1970,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
       if (done) break;
     }
     if (staged && tid == 0) issue_upto(Pm, smem, C, a, it + 1, it + C.n_stages, !sectioned);
-    exec_tile<VE>(Pm, P, sec, sec_n, T, L, lane, it, C, grand, A, rbuf, tb);
+    exec_tile<VE>(Pm, P, T, L, lane, it, C, grand, A, rbuf, tb, hmask);
     if (staged) it++;
     pos_next(P, T);
     if (sectioned) tau++;
