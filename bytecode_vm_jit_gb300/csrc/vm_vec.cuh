@@ -1787,6 +1787,74 @@ __device__ __forceinline__ void issue_upto(const LaunchParams& Pm, const uint8_t
   I.prog = prog;
 }
 
+// ---- the fast producer ----------------------------------------------------------
+// A launch of one plain rank <= 2 program whose stage loads are whole-row blocks of
+// row-major tensors (at most two) walks its tiles linearly: tile j of the CTA starts at
+// row (lo + j) * t0 of every tensor.  Its producer keeps everything in registers and
+// issues a tile with one expect-tx and one bulk copy per tensor.
+struct FastIssuer {
+  const uint8_t* src[2];  // tensor bases
+  uint32_t rowb[2];       // bytes of one row of each tensor (its row stride: row-major)
+  uint32_t dst[2];        // offsets in a stage
+  int n;                  // stage loads (1 or 2); 0 = not eligible
+  int lo, count;          // first tile of the CTA, tiles of the CTA
+  int t0, n0;             // rows per tile, rows of the iteration space
+  int issued;
+};
+__device__ __forceinline__ void fast_issue(FastIssuer& F, const Ctl& C, int need, int limit) {
+  while (F.issued < limit && F.issued < F.count && !*abort_flag()) {
+    const int stage = F.issued % C.n_stages;
+    const uint32_t parity = ((F.issued / C.n_stages) & 1) ^ 1;
+    if (F.issued >= need) {
+      if (!mbar_try_wait(bar_empty(stage), parity)) break;
+    } else if (!mbar_wait(bar_empty(stage), parity, C.st, abort_flag())) {
+      break;
+    }
+    const int r0 = (F.lo + F.issued) * F.t0;
+    const uint32_t nrows = (uint32_t)min(F.t0, F.n0 - r0);
+    uint8_t* base = dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes;
+    uint64_t* bar = bar_full(stage);
+    mbar_arrive_expect_tx(bar, nrows * (F.rowb[0] + (F.n > 1 ? F.rowb[1] : 0u)));
+    bulk_g2s(base + F.dst[0], F.src[0] + (size_t)r0 * F.rowb[0], nrows * F.rowb[0], bar);
+    if (F.n > 1) bulk_g2s(base + F.dst[1], F.src[1] + (size_t)r0 * F.rowb[1], nrows * F.rowb[1], bar);
+    F.issued++;
+  }
+}
+// set up the fast producer when the launch qualifies (every thread computes the same)
+__device__ __forceinline__ void fast_setup(FastIssuer& F, const Header* H, const Prog& P, const LaunchParams& Pm,
+                                           int lo, int hi) {
+  F.n = 0;
+  F.issued = 0;
+  if (H->n_progs != 1 || P.pr->kind != PK_VEC || P.r > 2 || P.tiles_in != 1) return;
+  const Instr* sec = P.body + 1;
+  const int sn = (int)P.body[0].imm;
+  int k = 0;
+  for (int i = 0; i < sn; i++) {
+    const Instr w = sec[i];
+    if (w.op != OP_LD || (w.flags & (LF_DMA | LF_FIRST | LF_HOIST)) != (LF_DMA | LF_FIRST)) continue;
+    const TensRec& T = P.tens[w.b];
+    const int esz = dtype_size(T.dtype);
+    if (k == 2 || (w.flags & LF_COLV) || (P.r == 2 && T.vs[0] != (int64_t)P.t_in)) return;  // not row-major blocks
+    // (constant indices keep the state in registers)
+    if (k == 0) {
+      F.src[0] = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
+      F.rowb[0] = (uint32_t)(P.t_in * esz);
+      F.dst[0] = w.aux0;
+    } else {
+      F.src[1] = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
+      F.rowb[1] = (uint32_t)(P.t_in * esz);
+      F.dst[1] = w.aux0;
+    }
+    k++;
+  }
+  if (k == 0) return;
+  F.n = k;
+  F.lo = lo;
+  F.count = hi - lo;
+  F.t0 = P.r == 2 ? P.t0 : 1;
+  F.n0 = P.r == 2 ? P.n0 : 1;
+}
+
 // ---- the kernel --------------------------------------------------------------
 // One walk over the CTA's work with a single tile-execution site: plain and stacked
 // launches over the concatenated tile range [lo, hi) across programs, sectioned
@@ -1864,6 +1932,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
   Lanes<VE> L;
   Prog P;
   TilePos T;
+  FastIssuer F;
+  F.n = 0;
+  F.issued = 0;
 
   int p = -1;        // plain: current program
   int g = lo;        // plain: next concatenated tile
@@ -1901,7 +1972,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
         staged = section_has_stage(sec, sec_n);
         tau = g - (int)P.pr->tile_base;
         pos_start(P, T, tau);
-        if (tid == 0 && it == 0) {
+        if (it == 0) fast_setup(F, H, P, Pm, lo, hi);
+        if (tid == 0 && it == 0 && !F.n) {
           Issuer& I = issuer();
           I.prog = p;
           I.g = g;
@@ -1969,7 +2041,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
       }
       if (done) break;
     }
-    if (staged && tid == 0) issue_upto(Pm, smem, C, a, it + 1, it + C.n_stages, !sectioned);
+    if (staged && tid == 0) {
+      if (F.n) fast_issue(F, C, it + 1, it + C.n_stages);
+      else issue_upto(Pm, smem, C, a, it + 1, it + C.n_stages, !sectioned);
+    }
     exec_tile<VE>(Pm, P, T, L, lane, it, C, grand, A, rbuf, tb, hmask);
     if (staged) it++;
     pos_next(P, T);
@@ -1979,7 +2054,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
   // copies still in flight land before the CTA exits (after an abort the consumers may
   // not have waited for them)
   if (tid == 0 && C.n_stages) {
-    const int issued = issuer().issued;
+    const int issued = F.n ? F.issued : issuer().issued;
     for (int j = issued > C.n_stages ? issued - C.n_stages : 0; j < issued; j++) {
       const unsigned long long t0 = globaltimer();
       while (!mbar_try_wait_sleep(bar_full(j % C.n_stages), (uint32_t)((j / C.n_stages) & 1), 20000u))
