@@ -4,8 +4,11 @@
 // (section 5.2) and the cube flow of its execution model (section 3.2, Fig 3); the
 // MindSpore DVM summary (section 3.3) describes the same cube-vector fusion.
 //
-// One persistent CTA per SM runs its contiguous tile range [c*body_tile,
-// min((c+1)*body_tile, block_dim)) (section 4.4).  A tile is 128 x t_N outputs.  Roles:
+// One persistent CTA per SM runs body_tile tiles (section 4.4).  Which tiles a core
+// takes does not change any result, so the kernel deals them round-robin (tiles c,
+// c + grid, c + 2*grid, ...): the tiles in flight at one time are neighbours in the
+// row-major tile grid and share their A and W blocks in L2, where contiguous ranges
+// would spread the working set over the whole of A.  A tile is 128 x t_N outputs.  Roles:
 //   warp 0, one lane   TMA producer: the A [128 x 64] and W [t_N x 64] k-blocks of each
 //                      tile go into a ring of shared-memory stages with the 128-byte
 //                      swizzle, completion counted on the stage's mbarrier;
@@ -372,9 +375,10 @@ __device__ void run_epilogue(const Instr* w, int nw, const TensRec* tens, void* 
 __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_constant__ CubeParams P) {
   const Header* H = reinterpret_cast<const Header*>(P.image);
   const int cta = blockIdx.x;
-  const int body_tile = (int)H->body_tile;
-  const int lo = cta * body_tile;
-  const int hi = min(lo + body_tile, (int)H->block_dim);
+  const int nblk = (int)H->block_dim;
+  const int step = (int)gridDim.x;
+  const int lo = cta;     // this CTA's tiles: lo, lo + step, ... < nblk
+  const int hi = nblk;
   if (lo >= hi) return;  // uniform over the CTA: nothing to do, nothing allocated
 
   extern __shared__ uint8_t cube_smem_raw[];
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
       tma_prefetch_map(&P.tmA);
       tma_prefetch_map(&P.tmW);
       int it = 0;
-      for (int tau = lo; tau < hi && !*abort; tau++) {
+      for (int tau = lo; tau < hi && !*abort; tau += step) {
         const int tm = tau / tiles_n, tn = tau - tm * tiles_n;
         for (int kb = 0; kb < nkb; kb++, it++) {
           const int s = it % S;
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
       const uint32_t idesc = mma_idesc(kBM, BN);
       int it = 0, jt = 0;
       bool issued = false;
-      for (int tau = lo; tau < hi && !*abort; tau++, jt++) {
+      for (int tau = lo; tau < hi && !*abort; tau += step, jt++) {
         const int b = jt & 1;
         const uint32_t use = (uint32_t)(jt >> 1);
         if (!mbar_wait(&C->tempty[b], (use & 1u) ^ 1u, st, abort)) break;
@@ -492,7 +496,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
     const int n_epi = (int)body[0].imm - 1;  // words after the MMA word
     const Instr* epi = body + 2;
     int jt = 0;
-    for (int tau = lo; tau < hi; tau++, jt++) {
+    for (int tau = lo; tau < hi; tau += step, jt++) {
       const int b = jt & 1;
       if (!mbar_wait(&C->tfull[b], (uint32_t)(jt >> 1) & 1u, st, abort)) break;
       tc_fence_after();
