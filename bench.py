@@ -484,16 +484,9 @@ def main():
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     gpu_launches = run.launches - launches0
-    t_local = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
-    ms_max = float(t_local.item())
-    if is_mm:
-        units = sum(wl.flops_of(m) for m in wl.sizes) * args.steps * world
-        value = units / (ms_max / 1e3) / 1e12
-    else:
-        units = wl.unit_bytes() * args.steps * world
-        value = units / (ms_max / 1e3) / 1e9
+    ms_max = max_over_ranks(ms, world, dev)
+    per_rank = sum(wl.flops_of(m) for m in wl.sizes) if is_mm else wl.unit_bytes()
+    value = job_throughput(per_rank * args.steps, world, ms_max, 1e12 if is_mm else 1e9)
     enc_us = [x / 1e3 for x in run.encode_ns]
     wall_us = [x / 1e3 for x in run.wall_ns]
 
@@ -563,6 +556,22 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time (every rank ran the same timed region between barriers)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max, scale):
+    """Whole-job rate: the units every replica processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3) / scale
 
 
 def percentile(xs, q):
