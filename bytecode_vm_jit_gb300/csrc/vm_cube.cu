@@ -64,6 +64,7 @@ struct CubeCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int n_ep;   // decoded epilogue micro-ops
 };
 static_assert(sizeof(CubeCtl) <= 256, "control block");
 
@@ -133,6 +134,25 @@ __host__ __device__ constexpr uint32_t mma_idesc(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// bounded wait without the suspend hint, for the roles on the MMA critical path (the
+// producer and the MMA issuer): a tight poll, with the clock and abort checked every 64
+// polls
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const DevStatus& st, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; i++)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > st.limit_ns) {
+      set_status(st.word, -100 /* DVM_E_TIMEOUT */);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // bounded wait that ignores the abort flag (draining copies and MMAs before exit)
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   const unsigned long long t0 = globaltimer();
@@ -154,19 +174,18 @@ __device__ __forceinline__ void st_elem(uint8_t* base, int dt, int64_t i, float 
 }
 
 // 32 values of (row m, columns n0..n0+31) of a bound tensor; columns >= n0+nvalid read 0
-__device__ __forceinline__ void ep_load(float (&x)[32], const TensRec& t, const uint8_t* base, int m, int n0,
-                                        int nvalid) {
-  const int dt = t.dtype;
+__device__ __forceinline__ void ep_load(float (&x)[32], int dt, int64_t vs0, int64_t vs1, const uint8_t* base, int m,
+                                        int n0, int nvalid) {
   const int esz = dtype_size(dt);
-  if (t.vs[1] == 0) {  // one value per row
-    const float v = ld_elem(base, dt, (int64_t)m * t.vs[0]);
+  if (vs1 == 0) {  // one value per row
+    const float v = ld_elem(base, dt, (int64_t)m * vs0);
 #pragma unroll
     for (int i = 0; i < 32; i++) x[i] = v;
     return;
   }
-  const int64_t off = (int64_t)m * t.vs[0] + (int64_t)n0 * t.vs[1];
+  const int64_t off = (int64_t)m * vs0 + (int64_t)n0 * vs1;
   const uint8_t* p = base + off * esz;
-  if (t.vs[1] == 1 && nvalid == 32 && ((uintptr_t)p & 15) == 0) {
+  if (vs1 == 1 && nvalid == 32 && ((uintptr_t)p & 15) == 0) {
     if (dt == DT_F32) {
 #pragma unroll
       for (int q = 0; q < 8; q++) {
@@ -194,16 +213,15 @@ __device__ __forceinline__ void ep_load(float (&x)[32], const TensRec& t, const 
     return;
   }
 #pragma unroll
-  for (int i = 0; i < 32; i++) x[i] = i < nvalid ? ld_elem(base, dt, off + (int64_t)i * t.vs[1]) : 0.f;
+  for (int i = 0; i < 32; i++) x[i] = i < nvalid ? ld_elem(base, dt, off + (int64_t)i * vs1) : 0.f;
 }
 
-__device__ __forceinline__ void ep_store(const float (&x)[32], const TensRec& t, uint8_t* base, int m, int n0,
-                                         int nvalid) {
-  const int dt = t.dtype;
+__device__ __forceinline__ void ep_store(const float (&x)[32], int dt, int64_t vs0, int64_t vs1, uint8_t* base, int m,
+                                         int n0, int nvalid) {
   const int esz = dtype_size(dt);
-  const int64_t off = (int64_t)m * t.vs[0] + (int64_t)n0 * t.vs[1];
+  const int64_t off = (int64_t)m * vs0 + (int64_t)n0 * vs1;
   uint8_t* p = base + off * esz;
-  if (t.vs[1] == 1 && nvalid == 32 && ((uintptr_t)p & 15) == 0) {
+  if (vs1 == 1 && nvalid == 32 && ((uintptr_t)p & 15) == 0) {
     if (dt == DT_F32) {
 #pragma unroll
       for (int q = 0; q < 8; q++)
@@ -227,7 +245,7 @@ __device__ __forceinline__ void ep_store(const float (&x)[32], const TensRec& t,
   }
 #pragma unroll
   for (int i = 0; i < 32; i++)
-    if (i < nvalid) st_elem(base, dt, off + (int64_t)i * t.vs[1], x[i]);
+    if (i < nvalid) st_elem(base, dt, off + (int64_t)i * vs1, x[i]);
 }
 
 __device__ __forceinline__ float ep_unary(int op, float x) {
@@ -300,50 +318,198 @@ __device__ __forceinline__ void put_slot(const float (&x)[32], int k, float (&ac
   }
 }
 
-// Run the epilogue words on 32 accumulator values of row m (valid when m < M), columns
-// n0..n0+nvalid-1.  Words are warp-uniform; loads and stores are skipped for rows
-// outside the output.
-__device__ void run_epilogue(const Instr* w, int nw, const TensRec* tens, void* const* ptrs, float (&acc)[32],
-                             int m, bool row_ok, int n0, int nvalid) {
-  float s1[32], s2[32], x[32];
-#pragma unroll
-  for (int i = 0; i < 32; i++) s1[i] = s2[i] = 0.f;
-  for (int k = 0; k < nw; k++) {
-    const Instr I = w[k];
+// ---- the epilogue, decoded once per CTA ---------------------------------------------
+// The epilogue words are decoded into micro-ops with their tensors resolved (base
+// pointer, strides, element type), and neighbours are fused so that a 32-column chunk
+// costs fewer dispatches: a load into a slot followed by a light op reading that slot
+// (when no later word reads the slot), a CASTBF followed by a store, and ops with an
+// immediate operand get their own handlers.
+enum EpHandler : uint8_t {
+  E_LD, E_ST, E_STB, E_MOV, E_BIN, E_OPLD_ADD, E_OPLD_SUB, E_OPLD_RSUB, E_OPLD_MUL,
+  E_ADDI, E_SUBI, E_RSUBI, E_MULI, E_ABS, E_NEG, E_CASTBF, E_UN, E_NOP
+};
+struct alignas(16) EpOp {
+  const uint8_t* base;  // tensor base (loads, stores)
+  int64_t vs0, vs1;     // element strides of the tensor over (row, column)
+  float imm;
+  uint8_t h, a, b, fl;
+  uint8_t dt, op, pad0, pad1;
+  uint32_t pad2;
+};
+static_assert(sizeof(EpOp) == 48, "epilogue micro-op");
+constexpr int kMaxEpOps = kMaxInstr;  // an epilogue never has more words than a body
+
+__device__ __forceinline__ bool ep_reads_slot(const Instr& w, int k) {
+  if (w.op == OP_MOV) return w.b == k;
+  if (w.op >= OP_ADD && w.op <= OP_POW) return !(w.flags & CF_IMM) && w.a == k;
+  return false;
+}
+__device__ __forceinline__ bool ep_slot_live_after(const Instr* w, int n, int i, int k) {
+  for (int j = i + 1; j < n; j++) {
+    if (ep_reads_slot(w[j], k)) return true;
+    if ((w[j].op == OP_LD || w[j].op == OP_MOV) && w[j].a == k) return false;
+  }
+  return false;
+}
+
+// decode (one thread); returns the number of micro-ops
+__device__ __forceinline__ int ep_decode(const Instr* w, int n, const TensRec* tens, void* const* ptrs, EpOp* E) {
+  int m = 0;
+  for (int i = 0; i < n && m < kMaxEpOps; i++) {
+    const Instr I = w[i];
+    EpOp e;
+    e.base = nullptr;
+    e.vs0 = e.vs1 = 0;
+    e.imm = __uint_as_float(I.imm);
+    e.h = E_NOP;
+    e.a = I.a;
+    e.b = I.b;
+    e.fl = I.flags;
+    e.dt = 0;
+    e.op = I.op;
+    const bool imm = I.flags & CF_IMM, rev = I.flags & CF_REV;
     switch (I.op) {
       case OP_LD: {
         const TensRec& t = tens[I.b];
-        if (row_ok) ep_load(x, t, static_cast<const uint8_t*>(ptrs[t.binding]), m, n0, nvalid);
-        else {
-#pragma unroll
-          for (int i = 0; i < 32; i++) x[i] = 0.f;
+        e.base = static_cast<const uint8_t*>(ptrs[t.binding]);
+        e.vs0 = t.vs[0];
+        e.vs1 = t.vs[1];
+        e.dt = t.dtype;
+        e.h = E_LD;
+        if (I.a != 0 && i + 1 < n) {
+          const Instr x = w[i + 1];
+          if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && !(x.flags & CF_IMM) && x.a == I.a &&
+              !ep_slot_live_after(w, n, i + 1, I.a)) {
+            e.h = x.op == OP_ADD ? E_OPLD_ADD : x.op == OP_MUL ? E_OPLD_MUL : (x.flags & CF_REV) ? E_OPLD_RSUB : E_OPLD_SUB;
+            i++;
+          }
         }
-        put_slot(x, I.a, acc, s1, s2);
         break;
       }
       case OP_ST: {
         const TensRec& t = tens[I.a];
-        if (row_ok) ep_store(acc, t, static_cast<uint8_t*>(ptrs[t.binding]), m, n0, nvalid);
+        e.base = static_cast<const uint8_t*>(ptrs[t.binding]);
+        e.vs0 = t.vs[0];
+        e.vs1 = t.vs[1];
+        e.dt = t.dtype;
+        e.h = E_ST;
         break;
       }
-      case OP_MOV:
-        sel_slot(x, I.b, acc, s1, s2);
-        put_slot(x, I.a, acc, s1, s2);
-        break;
-      case OP_BCAST:   // row values are held replicated across the 32 columns already
-      case OP_WAIT:
-      case OP_REL:
-        break;
-      case OP_ADD: case OP_SUB: case OP_MUL: case OP_DIV: case OP_MAX: case OP_MIN: case OP_POW: {
-        if (I.flags & CF_IMM) {
-          const float v = __uint_as_float(I.imm);
-#pragma unroll
-          for (int i = 0; i < 32; i++) x[i] = v;
-        } else {
-          sel_slot(x, I.a, acc, s1, s2);
+      case OP_CASTBF:
+        e.h = E_CASTBF;
+        if (i + 1 < n && w[i + 1].op == OP_ST) {
+          const TensRec& t = tens[w[i + 1].a];
+          e.base = static_cast<const uint8_t*>(ptrs[t.binding]);
+          e.vs0 = t.vs[0];
+          e.vs1 = t.vs[1];
+          e.dt = t.dtype;
+          e.h = E_STB;
+          i++;
         }
-        const bool rev = (I.flags & CF_REV) != 0;
-        switch (I.op) {
+        break;
+      case OP_MOV: e.h = E_MOV; break;
+      case OP_ADD: case OP_SUB: case OP_MUL:
+        if (imm) e.h = I.op == OP_ADD ? E_ADDI : I.op == OP_MUL ? E_MULI : rev ? E_RSUBI : E_SUBI;
+        else e.h = E_BIN;
+        break;
+      case OP_DIV: case OP_MAX: case OP_MIN: case OP_POW: e.h = E_BIN; break;
+      case OP_ABS: e.h = E_ABS; break;
+      case OP_NEG: e.h = E_NEG; break;
+      case OP_BCAST: case OP_WAIT: case OP_REL: e.h = E_NOP; break;
+      default: e.h = E_UN; break;
+    }
+    E[m++] = e;
+  }
+  return m;
+}
+
+// Run the epilogue micro-ops on 32 accumulator values of row m (valid when m < M),
+// columns n0..n0+nvalid-1.  Micro-ops are warp-uniform; loads and stores are skipped for
+// rows outside the output.
+__device__ void run_epilogue(const EpOp* E, int ne, float (&acc)[32], int m, bool row_ok, int n0, int nvalid) {
+  float s1[32], s2[32], x[32];
+#pragma unroll
+  for (int i = 0; i < 32; i++) s1[i] = s2[i] = 0.f;
+  for (int k = 0; k < ne; k++) {
+    const EpOp e = E[k];
+    switch (e.h) {
+      case E_LD:
+        if (row_ok) ep_load(x, e.dt, e.vs0, e.vs1, e.base, m, n0, nvalid);
+        else {
+#pragma unroll
+          for (int i = 0; i < 32; i++) x[i] = 0.f;
+        }
+        put_slot(x, e.a, acc, s1, s2);
+        break;
+      case E_OPLD_ADD: case E_OPLD_SUB: case E_OPLD_RSUB: case E_OPLD_MUL:
+        if (row_ok) ep_load(x, e.dt, e.vs0, e.vs1, e.base, m, n0, nvalid);
+        else {
+#pragma unroll
+          for (int i = 0; i < 32; i++) x[i] = 0.f;
+        }
+        if (e.h == E_OPLD_ADD) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) acc[i] = acc[i] + x[i];
+        } else if (e.h == E_OPLD_MUL) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) acc[i] = acc[i] * x[i];
+        } else if (e.h == E_OPLD_SUB) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) acc[i] = acc[i] - x[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i++) acc[i] = x[i] - acc[i];
+        }
+        break;
+      case E_ST:
+        if (row_ok) ep_store(acc, e.dt, e.vs0, e.vs1, const_cast<uint8_t*>(e.base), m, n0, nvalid);
+        break;
+      case E_STB:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = round_bf16(acc[i]);
+        if (row_ok) ep_store(acc, e.dt, e.vs0, e.vs1, const_cast<uint8_t*>(e.base), m, n0, nvalid);
+        break;
+      case E_MOV:
+        sel_slot(x, e.b, acc, s1, s2);
+        put_slot(x, e.a, acc, s1, s2);
+        break;
+      case E_ADDI:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = acc[i] + e.imm;
+        break;
+      case E_SUBI:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = acc[i] - e.imm;
+        break;
+      case E_RSUBI:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = e.imm - acc[i];
+        break;
+      case E_MULI:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = acc[i] * e.imm;
+        break;
+      case E_ABS:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = fabsf(acc[i]);
+        break;
+      case E_NEG:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = -acc[i];
+        break;
+      case E_CASTBF:
+#pragma unroll
+        for (int i = 0; i < 32; i++) acc[i] = round_bf16(acc[i]);
+        break;
+      case E_BIN: {
+        if (e.fl & CF_IMM) {
+#pragma unroll
+          for (int i = 0; i < 32; i++) x[i] = e.imm;
+        } else {
+          sel_slot(x, e.a, acc, s1, s2);
+        }
+        const bool rev = (e.fl & CF_REV) != 0;
+        switch (e.op) {
           case OP_ADD: ep_bin_loop<OP_ADD>(acc, x, rev); break;
           case OP_SUB: ep_bin_loop<OP_SUB>(acc, x, rev); break;
           case OP_MUL: ep_bin_loop<OP_MUL>(acc, x, rev); break;
@@ -354,19 +520,22 @@ __device__ void run_epilogue(const Instr* w, int nw, const TensRec* tens, void* 
         }
         break;
       }
-      case OP_SQRT: ep_un_loop<OP_SQRT>(acc); break;
-      case OP_ABS: ep_un_loop<OP_ABS>(acc); break;
-      case OP_LOG: ep_un_loop<OP_LOG>(acc); break;
-      case OP_EXP: ep_un_loop<OP_EXP>(acc); break;
-      case OP_ROUND: ep_un_loop<OP_ROUND>(acc); break;
-      case OP_FLOOR: ep_un_loop<OP_FLOOR>(acc); break;
-      case OP_ISFIN: ep_un_loop<OP_ISFIN>(acc); break;
-      case OP_NEG: ep_un_loop<OP_NEG>(acc); break;
-      case OP_RSQRT: ep_un_loop<OP_RSQRT>(acc); break;
-      case OP_RECIP: ep_un_loop<OP_RECIP>(acc); break;
-      case OP_SILU: ep_un_loop<OP_SILU>(acc); break;
-      case OP_CASTBF: ep_un_loop<OP_CASTBF>(acc); break;
-      default: break;  // the validator admits nothing else in a CUBE body
+      case E_UN:
+        switch (e.op) {
+          case OP_SQRT: ep_un_loop<OP_SQRT>(acc); break;
+          case OP_LOG: ep_un_loop<OP_LOG>(acc); break;
+          case OP_EXP: ep_un_loop<OP_EXP>(acc); break;
+          case OP_ROUND: ep_un_loop<OP_ROUND>(acc); break;
+          case OP_FLOOR: ep_un_loop<OP_FLOOR>(acc); break;
+          case OP_ISFIN: ep_un_loop<OP_ISFIN>(acc); break;
+          case OP_RSQRT: ep_un_loop<OP_RSQRT>(acc); break;
+          case OP_RECIP: ep_un_loop<OP_RECIP>(acc); break;
+          case OP_SILU: ep_un_loop<OP_SILU>(acc); break;
+          default: break;  // the validator admits nothing else in a CUBE body
+        }
+        break;
+      default:
+        break;
     }
   }
 }
@@ -387,7 +556,8 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
   const int S = H->n_stages;
   const uint32_t stage_bytes = H->stage_bytes;
   CubeCtl* C = reinterpret_cast<CubeCtl*>(smem + (size_t)S * stage_bytes);
-  uint8_t* img = smem + (size_t)S * stage_bytes + 256;
+  EpOp* eops = reinterpret_cast<EpOp*>(smem + (size_t)S * stage_bytes + 256);
+  uint8_t* img = smem + (size_t)S * stage_bytes + 256 + kMaxEpOps * sizeof(EpOp);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -441,7 +611,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
         for (int kb = 0; kb < nkb; kb++, it++) {
           const int s = it % S;
           const uint32_t ph = (uint32_t)(it / S) & 1u;
-          if (!mbar_wait(&C->empty[s], ph ^ 1u, st, abort)) break;
+          if (!mbar_spin(&C->empty[s], ph ^ 1u, st, abort)) break;
           mbar_arrive_expect_tx(&C->full[s], stage_bytes);
           const uint32_t a_dst = ring + (uint32_t)s * stage_bytes;
           tma_load_2d(a_dst, &P.tmA, kb * kBK, tm * kBM, &C->full[s]);
@@ -461,14 +631,14 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
       for (int tau = lo; tau < hi && !*abort; tau += step, jt++) {
         const int b = jt & 1;
         const uint32_t use = (uint32_t)(jt >> 1);
-        if (!mbar_wait(&C->tempty[b], (use & 1u) ^ 1u, st, abort)) break;
+        if (!mbar_spin(&C->tempty[b], (use & 1u) ^ 1u, st, abort)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * BNp);
         bool ok = true;
         for (int kb = 0; kb < nkb; kb++, it++) {
           const int s = it % S;
           const uint32_t ph = (uint32_t)(it / S) & 1u;
-          if (!mbar_wait(&C->full[s], ph, st, abort)) { ok = false; break; }
+          if (!mbar_spin(&C->full[s], ph, st, abort)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = ring + (uint32_t)s * stage_bytes;
           const uint64_t da = sw128_desc(a_addr), db = sw128_desc(a_addr + kBM * kBK * 2);
@@ -494,7 +664,10 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
     const Instr* body = reinterpret_cast<const Instr*>(img + spr->body_off);
     const TensRec* tens = reinterpret_cast<const TensRec*>(img + spr->tens_off);
     const int n_epi = (int)body[0].imm - 1;  // words after the MMA word
-    const Instr* epi = body + 2;
+    // decode the epilogue once (first epilogue thread), then sync the epilogue warps
+    if (threadIdx.x == 64) C->n_ep = ep_decode(body + 2, n_epi, tens, P.ptrs, eops);
+    named_bar(2, 128);
+    const int ne = C->n_ep;
     int jt = 0;
     for (int tau = lo; tau < hi; tau += step, jt++) {
       const int b = jt & 1;
@@ -508,7 +681,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
         if (n0 >= N) break;  // warp-uniform
         float acc[32];
         tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BNp + c), acc);
-        run_epilogue(epi, n_epi, tens, P.ptrs, acc, m, row_ok, n0, min(min(32, BN - c), N - n0));
+        run_epilogue(eops, ne, acc, m, row_ok, n0, min(min(32, BN - c), N - n0));
       }
       tc_fence_before();
       mbar_arrive(&C->tempty[b]);
@@ -599,7 +772,7 @@ int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* 
   for (int i = 0; i < n; i++) P.ptrs[i] = ptrs[i];
   P.status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(st->scratch) + 8);
   P.timeout_ns = (unsigned long long)st->timeout_ms * 1000000ull;
-  const size_t smem = 1024 + ring + 256 + P.image_len;
+  const size_t smem = 1024 + ring + 256 + kMaxEpOps * sizeof(EpOp) + P.image_len;
   if ((int)smem > st->max_smem_optin) {
     std::snprintf(msg, cap, "CUBE shared memory %zu exceeds the device limit %d", smem, st->max_smem_optin);
     return -8;
