@@ -363,9 +363,16 @@ struct Lanes {
   uint32_t seg;    // bit v: vector v maps to a segment of the tile
   uint32_t rowok;  // bit v: the segment's row lies inside the iteration space (per tile)
   int rw0, rw1;    // one-row programs: warps whose partials make up this thread's row
-  // tile row and first tile column of vector v (from the program's segment table)
-  __device__ __forceinline__ int row(int v) const { return segtab()[(s0 + v) & (kMaxSegs - 1)] >> 16; }
-  __device__ __forceinline__ int col(int v) const { return (segtab()[(s0 + v) & (kMaxSegs - 1)] & 0xffff) + lcol; }
+  bool ur;         // one-row program: the warp's segments are consecutive in one tile row
+  int row0, col0;  // one-row programs: that row, and vector 0's first column (with lcol)
+  // tile row and first tile column of vector v: arithmetic in one-row programs, else
+  // from the program's segment table
+  __device__ __forceinline__ int row(int v) const {
+    return ur ? row0 : (segtab()[(s0 + v) & (kMaxSegs - 1)] >> 16);
+  }
+  __device__ __forceinline__ int col(int v) const {
+    return ur ? col0 + v * (VE * 32) : (segtab()[(s0 + v) & (kMaxSegs - 1)] & 0xffff) + lcol;
+  }
   __device__ __forceinline__ static const int* segtab() { return reinterpret_cast<const int*>(dvm_smem + kSegOff); }
 };
 
@@ -393,14 +400,18 @@ __device__ __forceinline__ void fill_tables(const Prog& P) {
 // segments [w*nvu, (w+1)*nvu), one per vector of each lane.
 template <int VE>
 __device__ __forceinline__ void lanes_for_prog(const Prog& P, int warp, int lane, Lanes<VE>& L) {
+  const int a = VE * 32;
   L.s0 = warp * P.nvu;
   L.lcol = lane * VE;
   L.seg = 0;
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++)
     if (v < P.nvu && L.s0 + v < P.segs) L.seg |= 1u << v;
+  L.ur = P.ur;
+  L.row0 = min(L.s0 / P.m, kMaxRows - 1);
+  L.col0 = (L.s0 % P.m) * a + L.lcol;
   // one-row programs: the warps holding this thread's row
-  const int r = min(L.s0 / P.m, kMaxRows - 1);
+  const int r = L.row0;
   const int wl = (P.segs + P.nvu - 1) / P.nvu;
   L.rw0 = (r * P.m) / P.nvu;
   L.rw1 = min(((r + 1) * P.m + P.nvu - 1) / P.nvu, wl);
@@ -408,6 +419,10 @@ __device__ __forceinline__ void lanes_for_prog(const Prog& P, int warp, int lane
 
 template <int VE>
 __device__ __forceinline__ void lanes_for_tile(const Prog& P, const TilePos& O, Lanes<VE>& L) {
+  if (L.ur && P.r <= 2) {  // one row per thread: one comparison
+    L.rowok = (P.r < 2 || O.od[0] + L.row0 < P.n0) ? L.seg : 0u;
+    return;
+  }
   uint32_t ok = 0;
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
@@ -1103,6 +1118,16 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
         U[at].cnt++;
         i++;
       }
+      // a light op combining the result with a FULL slot (x - mean, xc * rstd, ...)
+      if (i + 1 < n) {
+        const Instr x = body[i + 1];
+        if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && (x.flags & CF_AROW) &&
+            !(x.flags & (CF_XROW | CF_IMM)) && x.a != 0) {
+          U[m++] = decode_word(P, body, i + 1, hoisted);
+          U[at].aux = 1;
+          i++;
+        }
+      }
       continue;
     }
     U[m++] = u;
@@ -1591,6 +1616,18 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         for (int v = 0; v < NV; v++) Q0[v] = q;
         __syncwarp();
         pc += u.cnt;
+        if (u.aux & 1) {  // the folded light op: ACC <- q op slot (FULL)
+          const Uop v = U[pc + 1];
+          tm_ld32(tm_slot(tb, v.a), X);
+          float av[NV];
+#pragma unroll
+          for (int j = 0; j < NV; j++) av[j] = q;
+          if (v.h == H_VADD_T) bin_vf_<VE, OP_ADD, false>(A, av, X);
+          else if (v.h == H_VMUL_T) bin_vf_<VE, OP_MUL, false>(A, av, X);
+          else if (v.h == H_VRSUB_T) bin_vf_<VE, OP_SUB, true>(A, av, X);
+          else bin_vf_<VE, OP_SUB, false>(A, av, X);
+          pc++;
+        }
         break;
       }
       case H_RRED_G: {
