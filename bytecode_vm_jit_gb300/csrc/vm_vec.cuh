@@ -221,30 +221,36 @@ __device__ __forceinline__ float* rowslot(int k, int warp) {
 }
 
 // =========================================================== DMA flow ==
-// Bulk copies of the hoisted (tile-invariant) loads of one program, at origin 0.
-// mode 0 counts bytes, mode 1 issues; the caller arms the mbarrier in between.
-__device__ __forceinline__ uint32_t dma_hoist(const LaunchParams& Pm, const Prog& P, uint8_t* dst_base, uint64_t* bar,
-                                              int mode) {
-  const int valid_in = min(P.t_in, P.n_in);
-  uint32_t total = 0;
-  const int n = (int)P.pr->body_len;
-  for (int i = 0; i < n; i++) {
-    const Instr w = P.body[i];
-    if (w.op != OP_LD || (w.flags & (LF_DMA | LF_FIRST | LF_HOIST)) != (LF_DMA | LF_FIRST | LF_HOIST)) continue;
-    const TensRec& T = P.tens[w.b];
-    const int esz = dtype_size(T.dtype);
-    const uint8_t* src = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
-    uint8_t* dst = dst_base + w.aux0;
-    const uint32_t bytes = (uint32_t)(valid_in * esz);
-    const int nrows = (w.flags & LF_COLV) ? 1 : P.rows;
-    for (int row = 0; row < nrows; row++) {
-      int64_t off = 0;
-      if (P.r > 1 && !row_off_div(P.pr, P.r, 0, 0, 0, row, T.vs, &off)) continue;
-      total += bytes;
-      if (mode) bulk_g2s(dst + (size_t)row * P.t_in * esz, src + off * esz, bytes, bar);
+// Bulk copies of the hoisted (tile-invariant) loads of every program, at origin 0, by
+// one warp: lane i takes words i, i+32, ...; each copy raises the barrier's transaction
+// count before it is issued, and lane 0 arrives once all lanes have issued theirs.
+__device__ __forceinline__ void dma_hoist_warp(const LaunchParams& Pm, const uint8_t* img, int n_progs, int a,
+                                               uint64_t* bar, int lane) {
+  for (int p = 0; p < n_progs; p++) {
+    Prog P;
+    load_prog(img, p, P, a);
+    const int valid_in = min(P.t_in, P.n_in);
+    uint8_t* dst_base = dvm_smem + kDataOff + P.pr->hoist_base;
+    const int n = (int)P.pr->body_len;
+    for (int i = lane; i < n; i += 32) {
+      const Instr w = P.body[i];
+      if (w.op != OP_LD || (w.flags & (LF_DMA | LF_FIRST | LF_HOIST)) != (LF_DMA | LF_FIRST | LF_HOIST)) continue;
+      const TensRec& T = P.tens[w.b];
+      const int esz = dtype_size(T.dtype);
+      const uint8_t* src = static_cast<const uint8_t*>(Pm.ptrs[T.binding]);
+      uint8_t* dst = dst_base + w.aux0;
+      const uint32_t bytes = (uint32_t)(valid_in * esz);
+      const int nrows = (w.flags & LF_COLV) ? 1 : P.rows;
+      for (int row = 0; row < nrows; row++) {
+        int64_t off = 0;
+        if (P.r > 1 && !row_off_div(P.pr, P.r, 0, 0, 0, row, T.vs, &off)) continue;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(dst + (size_t)row * P.t_in * esz, src + off * esz, bytes, bar);
+      }
     }
   }
-  return total;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 
 // Producer state, kept in shared memory (only thread 0 touches it).  The stage loads
@@ -667,6 +673,18 @@ __device__ __forceinline__ void stg_vectors_fast(const float (&acc)[REG], uint8_
 }
 
 // ---- element-wise math --------------------------------------------------------
+// The hardware square root (one MUFU operation, relative error near 2^-23) for whole
+// registers: the IEEE-rounded sqrtf adds a correction sequence and a special-value
+// branch per element, which dominated a FULL-register Sqrt.
+__device__ __forceinline__ float sqrt_hw(float x) {
+  float r;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// SiLU for whole registers from the hardware exponential and divide intrinsics
+// (error a few ulp; x < -87 gives -0 instead of a denormal)
+__device__ __forceinline__ float silu_hw(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
 __device__ __forceinline__ float unary_fn(int op, float x) {
   switch (op) {
     case OP_SQRT: return sqrtf(x);
@@ -997,25 +1015,6 @@ __device__ __forceinline__ Uop decode_word(const Prog& P, const Instr* body, int
   return u;
 }
 
-// does a word read FULL slot k?  (MOV from k, or a FULL binary operand in slot k)
-__device__ __forceinline__ bool reads_slot(const Instr& w, int k) {
-  if (w.op == OP_MOV) return !(w.flags & 1) && w.b == k;
-  if (w.op >= OP_ADD && w.op <= OP_POW) return !(w.flags & (CF_IMM | CF_XROW)) && w.a == k;
-  return false;
-}
-__device__ __forceinline__ bool writes_slot(const Instr& w, int k) {
-  if (w.op == OP_LD) return !(w.flags & LF_ROWV) && w.a == k;
-  if (w.op == OP_MOV) return !(w.flags & 1) && w.a == k;
-  return false;
-}
-// is FULL slot k read again after word i (before it is overwritten) within the section?
-__device__ __forceinline__ bool slot_live_after(const Instr* body, int n, int i, int k) {
-  for (int j = i + 1; j < n; j++) {
-    if (reads_slot(body[j], k)) return true;
-    if (writes_slot(body[j], k)) return false;
-  }
-  return false;
-}
 __device__ __forceinline__ bool is_load_uop(uint8_t h) { return h >= H_LD_S4 && h <= H_LD_G; }
 __device__ __forceinline__ bool is_row_scalar(const Instr& w) {
   if (w.op >= OP_ADD && w.op <= OP_POW) return (w.flags & CF_AROW) && (w.flags & (CF_XROW | CF_IMM));
@@ -1023,10 +1022,32 @@ __device__ __forceinline__ bool is_row_scalar(const Instr& w) {
   return false;
 }
 
-// decode a section (thread 0; the caller synchronises the CTA before and after)
+// decode a section (one thread of warp 1, so that thread 0 can start the first copies
+// meanwhile; the caller synchronises the CTA before and after)
+constexpr int kDecodeThread = 32;
 __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body, int n) {
-  if (threadIdx.x != 0) return;
+  if (threadIdx.x != kDecodeThread) return;
   Uop* U = uops();
+  // liveness of the FULL slots in one backward pass: bit k of live[j] says that slot k
+  // is read after word j before anything overwrites it (the row-reduction partials are
+  // free while a section is decoded)
+  uint8_t* live = reinterpret_cast<uint8_t*>(red_buf(0));
+  {
+    uint32_t lv = 0;
+    for (int j = n - 1; j >= 0; j--) {
+      live[j] = (uint8_t)lv;
+      const Instr w = body[j];
+      uint32_t wr = 0, rd = 0;
+      if (w.op == OP_LD && !(w.flags & LF_ROWV)) wr = 1u << w.a;
+      if (w.op == OP_MOV && !(w.flags & 1)) {
+        wr = 1u << w.a;
+        rd = 1u << w.b;
+      }
+      if (w.op >= OP_ADD && w.op <= OP_POW && !(w.flags & (CF_IMM | CF_XROW))) rd = 1u << w.a;
+      lv = (lv & ~wr) | rd;
+    }
+  }
+  auto slot_live_after = [&](const Instr*, int, int j, int k) { return ((live[j] >> k) & 1) != 0; };
   int m = 0, hoisted = 0;
   bool pend_wait = false;
   for (int i = 0; i < n; i++) {
@@ -1540,13 +1561,13 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         break;
       }
       case H_SQRT:
-        DVM_MAP(sqrtf(x))
+        DVM_MAP(sqrt_hw(x))
         break;
       case H_EXP:
         DVM_MAP(expf(x))
         break;
       case H_SILU:
-        DVM_MAP(x / (1.0f + expf(-x)))
+        DVM_MAP(silu_hw(x))
         break;
       case H_HEAVY_U:
         tm_st32(tm_scratch(tb), A);
@@ -1605,11 +1626,17 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         }
         float p = mx ? vmax(s0, s1) : s0 + s1;
         p = mx ? warp_reduce<true>(p) : warp_reduce<false>(p);
-        if (lane == 0 && L.seg) red[warp] = p;
-        consumer_sync();
-        float q = ident;
-        if (L.seg)
+        // only the warps of this thread's row take part: a warp that holds the whole row
+        // needs nobody, a group of warps meets at its own named barrier (ids 8..15, one
+        // per group start), so row groups run independently of each other
+        float q = p;
+        const int gw = L.rw1 - L.rw0;
+        if (gw > 1 && L.seg) {
+          if (lane == 0) red[warp] = p;
+          named_bar(8 + L.rw0, 32 * gw);
+          q = ident;
           for (int k = L.rw0; k < L.rw1; k++) q = mx ? vmax(q, red[k]) : q + red[k];
+        }
         if (u.cnt) q = row_fold(U + pc + 1, u.cnt, q, warp);
         __syncwarp();
 #pragma unroll
@@ -1935,19 +1962,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
   if (!has_work && !sectioned) return;
   const int n_progs = H->n_progs;
 
-  // hoisted (tile-invariant) loads: once per CTA, all programs, one mbarrier phase
-  if (tid == 0 && has_work && H->hoist_bytes) {
-    uint32_t total = 0;
-    for (int mode = 0; mode < 2; mode++) {
-      if (mode == 1) mbar_arrive_expect_tx(bar_hoist(), total);
-      for (int p = 0; p < n_progs; p++) {
-        Prog P;
-        load_prog(smem, p, P, a);
-        total += dma_hoist(Pm, P, hoist_area() + P.pr->hoist_base, bar_hoist(), mode);
-      }
-    }
-  }
-  if (H->hoist_bytes && has_work) mbar_wait(bar_hoist(), 0, C.st, abort_flag());
+  // hoisted (tile-invariant) loads: once per CTA, all programs, one mbarrier phase,
+  // issued by warp 2 after the TMEM allocation below; the consumers wait for them just
+  // before their first tile, so that the copies overlap the program setup
+  bool hoist_pending = H->hoist_bytes && has_work;
 
   // TMEM: the slots and scratch registers (warp 0 allocates and frees all columns)
   if (warp == 0) {
@@ -1958,6 +1976,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tm_base(*reinterpret_cast<volatile uint32_t*>(dvm_smem + kTmemOff));
+  if (warp == 2 && hoist_pending) dma_hoist_warp(Pm, smem, n_progs, a, bar_hoist(), lane);
 
   float A[REG];
 #pragma unroll
@@ -2002,25 +2021,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
         sec = P.body + 1;
         sec_n = (int)P.body[0].imm;
         __syncthreads();  // the previous program's tiles may still read the tables
+        staged = section_has_stage(sec, sec_n);
+        tau = g - (int)P.pr->tile_base;
+        pos_start(P, T, tau);
+        if (tid == 0 && it == 0) {
+          // the producer sets up and starts the first copies while another thread
+          // decodes the section
+          fast_setup(F, H, P, Pm, lo, hi);
+          if (!F.n) {
+            Issuer& I = issuer();
+            I.prog = p;
+            I.g = g;
+            I.g_end = hi;
+            dma_section(I, P, Pm, sec, sec_n);
+            I.tau = tau;
+            I.c0 = T.c0;
+            I.cin = T.cin;
+            I.issued = 0;
+          }
+          if (staged) {
+            if (F.n) fast_issue(F, C, 1, C.n_stages);
+            else issue_upto(Pm, smem, C, a, 1, C.n_stages, true);
+          }
+        }
         fill_tables<VE>(P);
         decode_section(P, sec, sec_n);
         hmask = 0;
         __syncthreads();
-        staged = section_has_stage(sec, sec_n);
-        tau = g - (int)P.pr->tile_base;
-        pos_start(P, T, tau);
-        if (it == 0) fast_setup(F, H, P, Pm, lo, hi);
-        if (tid == 0 && it == 0 && !F.n) {
-          Issuer& I = issuer();
-          I.prog = p;
-          I.g = g;
-          I.g_end = hi;
-          dma_section(I, P, Pm, sec, sec_n);
-          I.tau = tau;
-          I.c0 = T.c0;
-          I.cin = T.cin;
-          I.issued = 0;
-        }
       }
     } else {
       bool done = false;
@@ -2082,6 +2109,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
       if (F.n) fast_issue(F, C, it + 1, it + C.n_stages);
       else issue_upto(Pm, smem, C, a, it + 1, it + C.n_stages, !sectioned);
     }
+    if (hoist_pending) {
+      mbar_wait(bar_hoist(), 0, C.st, abort_flag());
+      hoist_pending = false;
+    }
     exec_tile<VE>(Pm, P, T, L, lane, it, C, grand, A, rbuf, tb, hmask);
     if (staged) it++;
     pos_next(P, T);
@@ -2089,7 +2120,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) vm_vec_kernel(const __grid_consta
     else g++;
   }
   // copies still in flight land before the CTA exits (after an abort the consumers may
-  // not have waited for them)
+  // not have waited for them; a CTA that ran no tile never waited for its hoisted loads)
+  if (tid == 0 && hoist_pending) mbar_wait(bar_hoist(), 0, C.st, abort_flag());
   if (tid == 0 && C.n_stages) {
     const int issued = F.n ? F.issued : issuer().issued;
     for (int j = issued > C.n_stages ? issued - C.n_stages : 0; j < issued; j++) {
