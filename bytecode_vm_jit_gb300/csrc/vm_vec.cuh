@@ -612,6 +612,13 @@ __device__ __forceinline__ float load_scalar(const uint8_t* base, int64_t off, i
 template <int VE, int ESZ>
 __device__ __forceinline__ void lds_vectors(float (&dst)[REG], const uint8_t* region, int rstride,
                                             const Lanes<VE>& L) {
+  if (L.ur) {  // one row: the vectors sit at constant offsets from the first one
+    const uint8_t* p = region + (size_t)(L.row0 * rstride + L.col0) * ESZ;
+#pragma unroll
+    for (int v = 0; v < Lanes<VE>::NV; v++)
+      if ((L.seg >> v) & 1u) unpack<VE, ESZ>(p + v * (VE * 32 * ESZ), dst + v * VE);
+    return;
+  }
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
     if (!((L.seg >> v) & 1u)) continue;   // warp-uniform
@@ -622,6 +629,13 @@ __device__ __forceinline__ void lds_vectors(float (&dst)[REG], const uint8_t* re
 template <int VE, int ESZ>
 __device__ __forceinline__ void ldg_vectors_fast(float (&dst)[REG], const uint8_t* base, int64_t vs0, int oin,
                                                  const TilePos& O, const Lanes<VE>& L) {
+  if (L.ur) {
+    const uint8_t* p = base + ((int64_t)(O.od[0] + L.row0) * vs0 + oin + L.col0) * ESZ;
+#pragma unroll
+    for (int v = 0; v < Lanes<VE>::NV; v++)
+      if ((L.seg >> v) & 1u) unpack<VE, ESZ>(p + v * (VE * 32 * ESZ), dst + v * VE);
+    return;
+  }
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
     if (!((L.seg >> v) & 1u)) continue;
@@ -664,6 +678,13 @@ __device__ __forceinline__ void pack_store(uint8_t* p, const float* s) {
 template <int VE, int ESZ>
 __device__ __forceinline__ void stg_vectors_fast(const float (&acc)[REG], uint8_t* base, int64_t vs0, int oin,
                                                  const TilePos& O, const Lanes<VE>& L) {
+  if (L.ur) {
+    uint8_t* p = base + ((int64_t)(O.od[0] + L.row0) * vs0 + oin + L.col0) * ESZ;
+#pragma unroll
+    for (int v = 0; v < Lanes<VE>::NV; v++)
+      if ((L.seg >> v) & 1u) pack_store<VE, ESZ>(p + v * (VE * 32 * ESZ), acc + v * VE);
+    return;
+  }
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
     if (!((L.seg >> v) & 1u)) continue;
@@ -1201,13 +1222,21 @@ __device__ __forceinline__ void row_unary(int op, float* dst, int nv, int nvall)
   }
 }
 // the ROW-scalar micro-ops folded into a reduction, applied to its one-row result
+// (the usual operators are tested first: a chain of uniform branches is much cheaper
+// than the jump of a runtime switch)
 __device__ __forceinline__ float row_fold(const Uop* F, int cnt, float q, int warp) {
 #pragma unroll 1
   for (int j = 0; j < cnt; j++) {
     const Uop v = F[j];
     if (v.h == H_ROWBIN) {
       const float x = (v.fl & CF_XROW) ? rowslot(v.a, warp)[0] : v.imm;
-      q = (v.fl & CF_REV) ? bin_rt(v.op, x, q) : bin_rt(v.op, q, x);
+      const bool rev = (v.fl & CF_REV) != 0;
+      const float l = rev ? x : q, r = rev ? q : x;
+      if (v.op == OP_MUL) q = l * r;
+      else if (v.op == OP_ADD) q = l + r;
+      else if (v.op == OP_SUB) q = l - r;
+      else if (v.op == OP_POW && r == -0.5f) q = l == 0.f ? __int_as_float(0x7f800000) : 1.0f / sqrtf(l);
+      else q = bin_rt(v.op, l, r);
     } else {
       q = unary_fn(v.op, q);
     }
@@ -1635,7 +1664,13 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
           if (lane == 0) red[warp] = p;
           named_bar(8 + L.rw0, 32 * gw);
           q = ident;
-          for (int k = L.rw0; k < L.rw1; k++) q = mx ? vmax(q, red[k]) : q + red[k];
+          // warp order, all loads issued together
+#pragma unroll
+          for (int k = 0; k < NW; k++)
+            if (k < gw) {
+              const float r = red[L.rw0 + k];
+              q = mx ? vmax(q, r) : q + r;
+            }
         }
         if (u.cnt) q = row_fold(U + pc + 1, u.cnt, q, warp);
         __syncwarp();
