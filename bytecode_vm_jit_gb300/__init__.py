@@ -10,6 +10,7 @@ The library is loaded on first use and must have been built for sm_103a
 """
 import ctypes
 import os
+import threading
 
 from . import build as _build
 
@@ -128,27 +129,54 @@ def dvm_reset(ctx):
     _check(ctx, lib().dvm_reset(ctx))
 
 
+class _Scratch(threading.local):
+    """Per-thread argument buffers reused across calls (the calls copy what they read)."""
+
+    def __init__(self):
+        self.sh = (ctypes.c_int64 * 8)()
+        self.st = (ctypes.c_int64 * 8)()
+        self.ins = (ctypes.c_int32 * 8)()
+        self.at = (ctypes.c_float * 8)()
+        self.out = ctypes.c_int32()
+        self.out_ref = ctypes.byref(self.out)
+        self.ptrs = (ctypes.c_void_p * MAX_BIND)()
+        self.ln = ctypes.c_size_t()
+        self.ln_ref = ctypes.byref(self.ln)
+        self.nt = ctypes.c_int32()
+        self.nt_ref = ctypes.byref(self.nt)
+
+
+_S = _Scratch()
+
+
+def _fill(buf, vals, ctype):
+    n = len(vals)
+    if n > len(buf):
+        return (ctype * n)(*vals)
+    buf[:n] = vals
+    return buf
+
+
 def dvm_input(ctx, dtype, shape, strides=None):
+    S = _S
     n = len(shape)
-    sh = (ctypes.c_int64 * n)(*shape)
-    st = (ctypes.c_int64 * n)(*strides) if strides is not None else None
-    out = ctypes.c_int32()
-    _check(ctx, lib().dvm_input(ctx, DTYPES[dtype], n, sh, st, ctypes.byref(out)))
-    return out.value
+    sh = _fill(S.sh, shape, ctypes.c_int64)
+    st = _fill(S.st, strides, ctypes.c_int64) if strides is not None else None
+    _check(ctx, lib().dvm_input(ctx, DTYPES[dtype], n, sh, st, S.out_ref))
+    return S.out.value
 
 
 def dvm_graph_add(ctx, op, inputs, dtype, attrs=(), shape=None):
-    code = OPS[op]
-    ins = (ctypes.c_int32 * max(1, len(inputs)))(*inputs)
+    S = _S
+    ins = _fill(S.ins, inputs, ctypes.c_int32)
     if shape is None:
         sh, rank = None, (0 if op == "opaque" else -1)
     else:
-        sh, rank = (ctypes.c_int64 * max(1, len(shape)))(*shape), len(shape)
-    at = (ctypes.c_float * max(1, len(attrs)))(*attrs)
-    out = ctypes.c_int32()
-    _check(ctx, lib().dvm_graph_add(ctx, code, ins, len(inputs), sh, rank, DTYPES[dtype], at, len(attrs),
-                                     ctypes.byref(out)))
-    return out.value
+        sh, rank = _fill(S.sh, shape, ctypes.c_int64), len(shape)
+    at = _fill(S.at, attrs, ctypes.c_float)
+    _check(ctx, lib().dvm_graph_add(ctx, OPS[op], ins, len(inputs), sh, rank, DTYPES[dtype], at, len(attrs),
+                                     S.out_ref))
+    return S.out.value
 
 
 def dvm_mark_output(ctx, vid):
@@ -163,9 +191,9 @@ def dvm_value_info(ctx, vid):
 
 
 def dvm_flush(ctx):
-    n = ctypes.c_int32()
-    _check(ctx, lib().dvm_flush(ctx, ctypes.byref(n)))
-    return n.value
+    S = _S
+    _check(ctx, lib().dvm_flush(ctx, S.out_ref))
+    return S.out.value
 
 
 _enc_buf = ctypes.create_string_buffer(MAX_IMAGE)
@@ -186,7 +214,7 @@ def dvm_validate(image):
 
 def dvm_run(ctx, image, ptrs, stream=None):
     n = len(ptrs)
-    arr = (ctypes.c_void_p * max(1, n))(*ptrs)
+    arr = _fill(_S.ptrs, ptrs, ctypes.c_void_p)
     _check(ctx, lib().dvm_run(ctx, image, len(image), arr, n, stream))
 
 
@@ -235,9 +263,15 @@ def _torch_dtype(code):
     return _TORCH_DT[code]
 
 
+_DT_NAMES = None
+
+
 def _dt_name(t):
-    import torch
-    return {torch.float32: "f32", torch.bfloat16: "bf16", torch.uint8: "u8"}[t.dtype]
+    global _DT_NAMES
+    if _DT_NAMES is None:
+        import torch
+        _DT_NAMES = {torch.float32: "f32", torch.bfloat16: "bf16", torch.uint8: "u8"}
+    return _DT_NAMES[t.dtype]
 
 
 class Ctx:
