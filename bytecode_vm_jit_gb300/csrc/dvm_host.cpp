@@ -1152,7 +1152,7 @@ static void default_desc(dvm_device_desc* d, int num_cores) {
   d->cap_elems = kCapElems;
   d->smem_budget = kSmemBudget;
   d->max_stages = 8;
-  d->c0_bytes = 4096;
+  d->c0_bytes = 65536;
   d->flops_per_byte = 280;
   d->n_slots = kNumSlots;
 }

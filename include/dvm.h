@@ -98,7 +98,7 @@ typedef struct {
   int32_t cap_elems;      /* padded elements per tile; default 8192 */
   int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 118784 */
   int32_t max_stages;     /* default 8 */
-  int32_t c0_bytes;       /* per-tile overhead of the cost model; default 4096 */
+  int32_t c0_bytes;       /* per-tile overhead of the cost model; default 65536 */
   int32_t flops_per_byte; /* cube cost-model balance; default 280 */
   int32_t n_slots;        /* register slots besides ACC; must be 2 */
 } dvm_device_desc;

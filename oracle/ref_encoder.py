@@ -54,7 +54,7 @@ MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
 CUBE_RING_BYTES = 196608   # shared-memory ring of the MatMul tile op (A and W k-blocks)
 
 DEFAULT_DESC = dict(num_cores=152, cap_elems=8192, smem_budget=187392, max_stages=8,
-                    c0_bytes=4096, flops_per_byte=280, n_slots=2)
+                    c0_bytes=65536, flops_per_byte=280, n_slots=2)
 
 
 class EncodeError(Exception):
