@@ -54,7 +54,8 @@ constexpr int kIssOff = kMiscOff + 128;                   // producer state (thr
 constexpr int kRowSlotOff = kIssOff + 384;                // ROW values of ACC, slots 1, 2: [slot][warp][8]
 constexpr int kTmemOff = kRowSlotOff + 3 * NW * 8 * 4;    // TMEM base address (ROW areas: 8 values per warp)
 constexpr int kUopOff = kTmemOff + 128;                   // decoded micro-ops of the current section
-constexpr int kDataOff = kUopOff + kMaxInstr * 16;        // hoist area, then the stage ring
+constexpr int kDecOff = kUopOff + kMaxInstr * 16;         // words decoded one per lane (scratch)
+constexpr int kDataOff = kDecOff + kMaxInstr * 16;        // hoist area, then the stage ring
 static_assert(kDataOff % 128 == 0, "data area alignment");
 static_assert(kDataOff + kSmemBudget <= 227 * 1024, "shared memory of the VEC interpreter");
 
@@ -322,6 +323,7 @@ __device__ __forceinline__ void issue_tile(const Issuer& Ds, int od0, int od1, i
   const TensRec* tens = Ds.tens;
   const int valid_in = min(t_in, Ds.n_in - o_in);
   const int nrows = r == 2 ? min(rows, Ds.n0 - od0) : 1;
+  const uint64_t pol = policy_stream();
   for (int mode = 0; mode < 2; mode++) {
     uint32_t total = 0;
     for (int k = 0; k < n; k++) {
@@ -331,7 +333,7 @@ __device__ __forceinline__ void issue_tile(const Issuer& Ds, int od0, int od1, i
       if (e.kind == 1 && valid_in == t_in) {  // whole rows: one contiguous block
         const uint32_t bytes = (uint32_t)nrows * t_in * e.esz;
         total += bytes;
-        if (mode) bulk_g2s(dst, e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz, bytes, bar);
+        if (mode) bulk_g2s_stream(dst, e.src + ((int64_t)od0 * e.vs0 + o_in) * e.esz, bytes, bar, pol);
       } else if (e.kind == 0) {  // one row shared by the tile (outer strides 0 within the tile)
         int64_t off = 0;
         bool ok = true;
@@ -346,13 +348,13 @@ __device__ __forceinline__ void issue_tile(const Issuer& Ds, int od0, int od1, i
         total += rowb * nrows;
         if (mode)
           for (int row = 0; row < nrows; row++)
-            bulk_g2s(dst + (size_t)row * t_in * e.esz, src + (int64_t)row * e.vs0 * e.esz, rowb, bar);
+            bulk_g2s_stream(dst + (size_t)row * t_in * e.esz, src + (int64_t)row * e.vs0 * e.esz, rowb, bar, pol);
       } else {  // rank > 2
         for (int row = 0; row < rows; row++) {
           int64_t off;
           if (!row_off_div(pr, r, od0, od1, od2, row, tens[e.tens].vs, &off)) continue;
           total += rowb;
-          if (mode) bulk_g2s(dst + (size_t)row * t_in * e.esz, e.src + (off + o_in) * e.esz, rowb, bar);
+          if (mode) bulk_g2s_stream(dst + (size_t)row * t_in * e.esz, e.src + (off + o_in) * e.esz, rowb, bar, pol);
         }
       }
     }
@@ -652,44 +654,42 @@ __device__ __forceinline__ void store_scalar(uint8_t* base, int64_t off, int dt,
 }
 
 template <int VE, int ESZ>
-__device__ __forceinline__ void pack_store(uint8_t* p, const float* s) {
+// 16-byte vector stores of tile results, marked for early L2 eviction (see policy_stream)
+__device__ __forceinline__ void pack_store(uint8_t* p, const float* s, uint64_t pol) {
   if constexpr (ESZ == 4) {
 #pragma unroll
     for (int q = 0; q < VE / 4; q++)
-      reinterpret_cast<float4*>(p)[q] = make_float4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
+      stg16_stream(p + 16 * q, __float_as_uint(s[4 * q]), __float_as_uint(s[4 * q + 1]), __float_as_uint(s[4 * q + 2]),
+                   __float_as_uint(s[4 * q + 3]), pol);
   } else if constexpr (ESZ == 2) {
 #pragma unroll
-    for (int q = 0; q < VE / 8; q++) {
-      uint4 u;
-      u.x = pack_bf16(s[8 * q], s[8 * q + 1]);
-      u.y = pack_bf16(s[8 * q + 2], s[8 * q + 3]);
-      u.z = pack_bf16(s[8 * q + 4], s[8 * q + 5]);
-      u.w = pack_bf16(s[8 * q + 6], s[8 * q + 7]);
-      reinterpret_cast<uint4*>(p)[q] = u;
-    }
+    for (int q = 0; q < VE / 8; q++)
+      stg16_stream(p + 16 * q, pack_bf16(s[8 * q], s[8 * q + 1]), pack_bf16(s[8 * q + 2], s[8 * q + 3]),
+                   pack_bf16(s[8 * q + 4], s[8 * q + 5]), pack_bf16(s[8 * q + 6], s[8 * q + 7]), pol);
   } else {
     uint32_t w4[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int e = 0; e < 16; e++) w4[e / 4] |= (uint32_t)(s[e] != 0.f ? 1 : 0) << (8 * (e % 4));
-    *reinterpret_cast<uint4*>(p) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    stg16_stream(p, w4[0], w4[1], w4[2], w4[3], pol);
   }
 }
 
 template <int VE, int ESZ>
 __device__ __forceinline__ void stg_vectors_fast(const float (&acc)[REG], uint8_t* base, int64_t vs0, int oin,
                                                  const TilePos& O, const Lanes<VE>& L) {
+  const uint64_t pol = policy_stream();
   if (L.ur) {
     uint8_t* p = base + ((int64_t)(O.od[0] + L.row0) * vs0 + oin + L.col0) * ESZ;
 #pragma unroll
     for (int v = 0; v < Lanes<VE>::NV; v++)
-      if ((L.seg >> v) & 1u) pack_store<VE, ESZ>(p + v * (VE * 32 * ESZ), acc + v * VE);
+      if ((L.seg >> v) & 1u) pack_store<VE, ESZ>(p + v * (VE * 32 * ESZ), acc + v * VE, pol);
     return;
   }
 #pragma unroll
   for (int v = 0; v < Lanes<VE>::NV; v++) {
     if (!((L.seg >> v) & 1u)) continue;
     const int64_t off = (int64_t)(O.od[0] + L.row(v)) * vs0 + oin + L.col(v);
-    pack_store<VE, ESZ>(base + off * ESZ, acc + v * VE);
+    pack_store<VE, ESZ>(base + off * ESZ, acc + v * VE, pol);
   }
 }
 
@@ -1043,33 +1043,71 @@ __device__ __forceinline__ bool is_row_scalar(const Instr& w) {
   return false;
 }
 
-// decode a section (one thread of warp 1, so that thread 0 can start the first copies
-// meanwhile; the caller synchronises the CTA before and after)
-constexpr int kDecodeThread = 32;
+// Decode a section (warp 1, while thread 0 starts the first copies; the caller
+// synchronises the CTA before and after).  The lanes decode one word each and work out
+// the slot liveness with ballots; lane 0 then makes the fusion pass over the decoded
+// words, which is the only sequential part.
+constexpr int kDecodeWarp = 1;
 __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body, int n) {
-  if (threadIdx.x != kDecodeThread) return;
+  if ((threadIdx.x >> 5) != kDecodeWarp) return;
+  const int lane = threadIdx.x & 31;
   Uop* U = uops();
-  // liveness of the FULL slots in one backward pass: bit k of live[j] says that slot k
-  // is read after word j before anything overwrites it (the row-reduction partials are
-  // free while a section is decoded)
+  Uop* Ut = reinterpret_cast<Uop*>(dvm_smem + kDecOff);
+  // bit k of live[j]: FULL slot k is read after word j before anything overwrites it
+  // (the row-reduction partials are free while a section is decoded)
   uint8_t* live = reinterpret_cast<uint8_t*>(red_buf(0));
   {
-    uint32_t lv = 0;
-    for (int j = n - 1; j >= 0; j--) {
-      live[j] = (uint8_t)lv;
-      const Instr w = body[j];
-      uint32_t wr = 0, rd = 0;
-      if (w.op == OP_LD && !(w.flags & LF_ROWV)) wr = 1u << w.a;
-      if (w.op == OP_MOV && !(w.flags & 1)) {
-        wr = 1u << w.a;
-        rd = 1u << w.b;
+    // words in order, 32 at a time: the hoisted-load index of a word counts the hoisted
+    // DMA loads before it
+    int carry = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      bool hz = false;
+      if (i < n) {
+        const Instr w = body[i];
+        hz = w.op == OP_LD && !(w.flags & LF_ROWV) && (w.flags & (LF_DMA | LF_HOIST)) == (LF_DMA | LF_HOIST);
       }
-      if (w.op >= OP_ADD && w.op <= OP_POW && !(w.flags & (CF_IMM | CF_XROW))) rd = 1u << w.a;
-      lv = (lv & ~wr) | rd;
+      const unsigned hm = __ballot_sync(~0u, hz);
+      int hoisted = carry + __popc(hm & ((1u << lane) - 1u));
+      if (i < n) Ut[i] = decode_word(P, body, i, hoisted);
+      carry += __popc(hm);
+    }
+    // liveness, last chunk first: the first later word that touches slot k decides
+    // (a word that reads and writes k counts as a read)
+    uint32_t live_in = 0;   // liveness at the start of the chunk after this one
+    for (int base = ((n - 1) & ~31); base >= 0; base -= 32) {
+      const int j = base + lane;
+      uint32_t rd = 0, wr = 0;
+      if (j < n) {
+        const Instr w = body[j];
+        if (w.op == OP_LD && !(w.flags & LF_ROWV)) wr = 1u << w.a;
+        if (w.op == OP_MOV && !(w.flags & 1)) {
+          wr = 1u << w.a;
+          rd = 1u << w.b;
+        }
+        if (w.op >= OP_ADD && w.op <= OP_POW && !(w.flags & (CF_IMM | CF_XROW))) rd = 1u << w.a;
+      }
+      const unsigned later = lane == 31 ? 0u : ~0u << (lane + 1);
+      uint32_t lv = 0, lin = live_in;
+#pragma unroll
+      for (int k = 1; k <= kNumSlots; k++) {
+        const unsigned R = __ballot_sync(~0u, (rd >> k) & 1u), Wm = __ballot_sync(~0u, (wr >> k) & 1u);
+        const unsigned t = (R | Wm) & later;
+        const bool lk = t ? ((R >> (__ffs(t) - 1)) & 1u) : ((live_in >> k) & 1u);
+        lv |= (uint32_t)lk << k;
+        // liveness at the start of this chunk, for the chunk before it
+        const unsigned t0 = R | Wm;
+        const bool l0 = t0 ? ((R >> (__ffs(t0) - 1)) & 1u) : ((live_in >> k) & 1u);
+        lin = (lin & ~(1u << k)) | ((uint32_t)l0 << k);
+      }
+      if (j < n) live[j] = (uint8_t)lv;
+      live_in = lin;
     }
   }
+  __syncwarp();
+  if (lane != 0) return;
   auto slot_live_after = [&](const Instr*, int, int j, int k) { return ((live[j] >> k) & 1) != 0; };
-  int m = 0, hoisted = 0;
+  int m = 0;
   bool pend_wait = false;
   for (int i = 0; i < n; i++) {
     const Instr w = body[i];
@@ -1081,12 +1119,12 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
       if (m > 0 && is_load_uop(U[m - 1].h) && (U[m - 1].fl & LF_DMA) && !(U[m - 1].fl & LF_HOIST)) {
         U[m - 1].uf |= UF_REL;
       } else {
-        Uop r = decode_word(P, body, i, hoisted);
+        Uop r = Ut[i];
         U[m++] = r;
       }
       continue;
     }
-    Uop u = decode_word(P, body, i, hoisted);
+    Uop u = Ut[i];
     if (pend_wait) {
       if (is_load_uop(u.h) && (u.fl & LF_DMA) && !(u.fl & LF_HOIST)) {
         u.uf |= UF_WAIT;
@@ -1136,7 +1174,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
       const Instr x = body[i + 1];
       if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && x.a == w.a &&
           !(x.flags & (CF_AROW | CF_XROW | CF_IMM))) {
-        Uop v = decode_word(P, body, i + 1, hoisted);
+        Uop v = Ut[i + 1];
         v.h = light_handler(x.op, 1, (x.flags & CF_REV) != 0);
         if (slot_live_after(body, n, i + 1, w.a)) v.uf |= UF_SAVE;
         U[m++] = v;
@@ -1145,7 +1183,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
       }
     }
     if (u.h == H_CASTBF && i + 1 < n && body[i + 1].op == OP_ST && !(body[i + 1].flags & LF_ROWV)) {
-      Uop v = decode_word(P, body, i + 1, hoisted);
+      Uop v = Ut[i + 1];
       v.uf |= UF_CAST;
       U[m++] = v;
       i++;
@@ -1156,7 +1194,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
       U[m++] = u;
       const int at = m - 1;
       while (i + 1 < n && is_row_scalar(body[i + 1]) && U[at].cnt < 8) {
-        U[m++] = decode_word(P, body, i + 1, hoisted);
+        U[m++] = Ut[i + 1];
         U[at].cnt++;
         i++;
       }
@@ -1165,7 +1203,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
         const Instr x = body[i + 1];
         if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && (x.flags & CF_AROW) &&
             !(x.flags & (CF_XROW | CF_IMM)) && x.a != 0) {
-          U[m++] = decode_word(P, body, i + 1, hoisted);
+          U[m++] = Ut[i + 1];
           U[at].aux = 1;
           i++;
         }
@@ -1914,8 +1952,9 @@ __device__ __forceinline__ void fast_issue(FastIssuer& F, const Ctl& C, int need
     uint8_t* base = dvm_smem + C.ring_off + (size_t)stage * C.stage_bytes;
     uint64_t* bar = bar_full(stage);
     mbar_arrive_expect_tx(bar, nrows * (F.rowb[0] + (F.n > 1 ? F.rowb[1] : 0u)));
-    bulk_g2s(base + F.dst[0], F.src[0] + (size_t)r0 * F.rowb[0], nrows * F.rowb[0], bar);
-    if (F.n > 1) bulk_g2s(base + F.dst[1], F.src[1] + (size_t)r0 * F.rowb[1], nrows * F.rowb[1], bar);
+    const uint64_t pol = policy_stream();
+    bulk_g2s_stream(base + F.dst[0], F.src[0] + (size_t)r0 * F.rowb[0], nrows * F.rowb[0], bar, pol);
+    if (F.n > 1) bulk_g2s_stream(base + F.dst[1], F.src[1] + (size_t)r0 * F.rowb[1], nrows * F.rowb[1], bar, pol);
     F.issued++;
   }
 }
