@@ -1109,7 +1109,6 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
   auto slot_live_after = [&](const Instr*, int, int j, int k) { return ((live[j] >> k) & 1) != 0; };
   int m = 0;
   bool pend_wait = false;
-  int sq_pending = 0;   // 1 + the slot to save (0 = none) for a square folded into the next reduction
   for (int i = 0; i < n; i++) {
     const Instr w = body[i];
     if (w.op == OP_WAIT) {
@@ -1177,14 +1176,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
           !(x.flags & (CF_AROW | CF_XROW | CF_IMM))) {
         Uop v = Ut[i + 1];
         v.h = light_handler(x.op, 1, (x.flags & CF_REV) != 0);
-        const bool save = slot_live_after(body, n, i + 1, w.a);
-        if (x.op == OP_MUL && P.ur && i + 2 < n && body[i + 2].op == OP_RSUM) {
-          // ... ; RSUM  ==>  the reduction squares (and saves ACC first)
-          sq_pending = 1 + (save ? w.a : 0);
-          i++;
-          continue;
-        }
-        if (save) v.uf |= UF_SAVE;
+        if (slot_live_after(body, n, i + 1, w.a)) v.uf |= UF_SAVE;
         U[m++] = v;
         i++;
         continue;
@@ -1198,14 +1190,6 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
       continue;
     }
     if ((u.h == H_RSUM_U || u.h == H_RMAX_U) && P.ur) {
-      if (sq_pending) {
-        u.aux |= 2;
-        if (sq_pending > 1) {
-          u.aux |= 4;
-          u.b = (uint8_t)(sq_pending - 1);
-        }
-        sq_pending = 0;
-      }
       // fold the ROW-scalar ops that follow (they act on this reduction's result)
       U[m++] = u;
       const int at = m - 1;
@@ -1220,7 +1204,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
         if ((x.op == OP_ADD || x.op == OP_SUB || x.op == OP_MUL) && (x.flags & CF_AROW) &&
             !(x.flags & (CF_XROW | CF_IMM)) && x.a != 0) {
           U[m++] = Ut[i + 1];
-          U[at].aux |= 1;
+          U[at].aux = 1;
           i++;
         }
       }
@@ -1235,12 +1219,6 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
     wt.cnt = 0;
     U[m++] = wt;
   }
-  // a load followed by a load or a store runs the next one without a dispatch
-  for (int j = 0; j + 1 < m; j++)
-    if (is_load_uop(U[j].h) && U[j].cnt == 0) {
-      if (is_load_uop(U[j + 1].h)) U[j].cnt = 1;
-      else if (U[j + 1].h == H_ST) U[j].cnt = 2;
-    }
   *uop_count() = m;
 }
 
@@ -1415,19 +1393,17 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
       case H_LD_S1:
       case H_LD_H:
       case H_LD_G: {
-        Uop lu = u;
-      next_load:
-        if (lu.uf & UF_WAIT) mbar_wait(bar_full(stage), parity, C.st, abort_flag());
-        if (lu.h == H_LD_G) {
-          ldg_full<VE>(X, P.tens[lu.b], P, L, O, Pm, tb, full);
+        if (u.uf & UF_WAIT) mbar_wait(bar_full(stage), parity, C.st, abort_flag());
+        if (u.h == H_LD_G) {
+          ldg_full<VE>(X, P.tens[u.b], P, L, O, Pm, tb, full);
         } else {
-          const int rs = (lu.fl & LF_COLV) ? 0 : P.t_in;
-          const uint8_t* region = ((lu.fl & LF_HOIST) ? dvm_smem : stage_base) + lu.off;
-          const int k = lu.aux >> 4;
-          if (lu.h == H_LD_H && (hmask & (1u << k))) {
+          const int rs = (u.fl & LF_COLV) ? 0 : P.t_in;
+          const uint8_t* region = ((u.fl & LF_HOIST) ? dvm_smem : stage_base) + u.off;
+          const int k = u.aux >> 4;
+          if (u.h == H_LD_H && (hmask & (1u << k))) {
             tm_ld32(tm_hoist(tb, k), X);
           } else {
-            const int esz = lu.h == H_LD_S4 ? 4 : lu.h == H_LD_S2 ? 2 : lu.h == H_LD_S1 ? 1 : (lu.aux & 15);
+            const int esz = u.h == H_LD_S4 ? 4 : u.h == H_LD_S2 ? 2 : u.h == H_LD_S1 ? 1 : (u.aux & 15);
             if (esz == 4) {
               lds_vectors<VE, 4>(X, region, rs, L);
             } else if (esz == 2) {
@@ -1435,35 +1411,25 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
             } else {
               if constexpr (VE == 16) lds_vectors<VE, 1>(X, region, rs, L);
             }
-            if (lu.h == H_LD_H) {
+            if (u.h == H_LD_H) {
               tm_st32(tm_hoist(tb, k), X);
               hmask |= 1u << k;
             }
           }
         }
-        if (lu.uf & UF_REL) {
+        if (u.uf & UF_REL) {
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_empty(stage));
         }
-        if (lu.uf & UF_STORE) tm_st32(tm_slot(tb, lu.a), X);
-        if (lu.uf & UF_OP) {
-          if (lu.op == OP_ADD) bin_ff_<OP_ADD, false>(A, X);
-          else if (lu.op == OP_MUL) bin_ff_<OP_MUL, false>(A, X);
-          else if (lu.uf & UF_REV) bin_ff_<OP_SUB, true>(A, X);
+        if (u.uf & UF_STORE) tm_st32(tm_slot(tb, u.a), X);
+        if (u.uf & UF_OP) {
+          if (u.op == OP_ADD) bin_ff_<OP_ADD, false>(A, X);
+          else if (u.op == OP_MUL) bin_ff_<OP_MUL, false>(A, X);
+          else if (u.uf & UF_REV) bin_ff_<OP_SUB, true>(A, X);
           else bin_ff_<OP_SUB, false>(A, X);
-        } else if (lu.uf & UF_TOACC) {
+        } else if (u.uf & UF_TOACC) {
 #pragma unroll
           for (int e = 0; e < REG; e++) A[e] = X[e];
-        }
-        // a load or a store that follows runs here, without a dispatch
-        if (lu.cnt == 1) {
-          lu = U[++pc];
-          goto next_load;
-        }
-        if (lu.cnt == 2) {
-          const Uop su = U[++pc];
-          if (su.uf & UF_CAST) DVM_MAP(round_bf16(x))
-          st_full<VE>(A, P.tens[su.a], P, L, O, Pm, tb, full);
         }
         break;
       }
@@ -1705,20 +1671,7 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         float* red = red_buf(rbuf);
         rbuf ^= 1;
         float s0 = ident, s1 = ident;
-        // folded "slot b <- ACC; ACC <- ACC * ACC": the sum squares as it adds
-        if (u.aux & 4) tm_st32(tm_slot(tb, u.b), A);
-        if (u.aux & 2) {
-#pragma unroll
-          for (int v = 0; v < NV; v++) {
-            if (!(((full ? L.seg : L.rowok) >> v) & 1u)) continue;
-            const int nc = full ? VE : ncol<VE>(P, O, L, v);
-#pragma unroll
-            for (int e = 0; e < VE; e += 2) {
-              if (e < nc) s0 += A[v * VE + e] * A[v * VE + e];
-              if (e + 1 < nc) s1 += A[v * VE + e + 1] * A[v * VE + e + 1];
-            }
-          }
-        } else if (full) {
+        if (full) {
 #pragma unroll
           for (int v = 0; v < NV; v++) {
             if (!((L.seg >> v) & 1u)) continue;
