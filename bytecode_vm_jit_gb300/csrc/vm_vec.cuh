@@ -1886,7 +1886,7 @@ __device__ __forceinline__ void issue_upto(const LaunchParams& Pm, const uint8_t
     const int stage = issued % C.n_stages;
     const uint32_t parity = ((issued / C.n_stages) & 1) ^ 1;
     if (issued >= need) {
-      if (!mbar_try_wait(bar_empty(stage), parity)) break;  // not free yet: try again next tile
+      if (!mbar_test_wait(bar_empty(stage), parity)) break;  // not free yet: try again next tile
     } else if (!mbar_wait(bar_empty(stage), parity, C.st, abort_flag())) {
       break;
     }
@@ -1943,7 +1943,7 @@ __device__ __forceinline__ void fast_issue(FastIssuer& F, const Ctl& C, int need
     const int stage = F.issued % C.n_stages;
     const uint32_t parity = ((F.issued / C.n_stages) & 1) ^ 1;
     if (F.issued >= need) {
-      if (!mbar_try_wait(bar_empty(stage), parity)) break;
+      if (!mbar_test_wait(bar_empty(stage), parity)) break;
     } else if (!mbar_wait(bar_empty(stage), parity, C.st, abort_flag())) {
       break;
     }
