@@ -112,7 +112,7 @@ def dvm_create(device=0):
 
 
 def dvm_create_host(**desc):
-    d = DeviceDesc(num_cores=152, cap_elems=8192, smem_budget=187392, max_stages=8, c0_bytes=65536,
+    d = DeviceDesc(num_cores=152, cap_elems=16384, smem_budget=187392, max_stages=8, c0_bytes=65536,
                    flops_per_byte=280, n_slots=2)
     for k, v in desc.items():
         setattr(d, k, int(v))

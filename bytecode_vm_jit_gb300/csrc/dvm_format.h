@@ -27,8 +27,8 @@ constexpr int kMaxInstr = 96;
 constexpr int kMaxImage = 8192;
 constexpr int kNumSlots = 2;        // addressable register slots besides ACC
 constexpr int kVmWarps = 8;         // warps of the VEC interpreter
-constexpr int kVmReg = 32;          // fp32 values in ACC (and per slot) per thread
-constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 8192 padded elements per tile
+constexpr int kVmReg = 64;          // fp32 values in ACC (and per slot) per thread
+constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 16384 padded elements per tile
 constexpr int kSmemBudget = 187392;  // DMA ring + hoist area of the VEC interpreter
 constexpr int kCubeRingBytes = 196608;  // TMA ring (A and W k-blocks) of the CUBE kernel
 constexpr int kMaxRank = 4;

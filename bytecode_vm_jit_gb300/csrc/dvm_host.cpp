@@ -745,6 +745,16 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
   int64_t best_t[4] = {0, 0, 0, 0};
   bool have = false;
   int64_t best_cost = 0;
+  int best_mis = 0;
+  // plans whose rows map whole onto the interpreter's warps come first: the tile has
+  // one row, or each warp's contiguous block of segments lies inside one row
+  auto warp_aligned = [&](const int64_t* cand) {
+    int64_t rows = 1;
+    for (int d = 0; d < r - 1; d++) rows *= cand[d];
+    const int64_t m = cand[r - 1] / p.a;
+    const int64_t nvu = cdiv(rows * m, kVmWarps);
+    return rows == 1 || (m >= nvu && m % nvu == 0);
+  };
   auto consider = [&](const int64_t* cand) {
     int64_t rows = 1;
     for (int d = 0; d < r - 1; d++) rows *= cand[d];
@@ -767,9 +777,11 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
       tb += dtype_size(tn.dtype) * cover;
     }
     int64_t cost = waves * (D.c0_bytes + tb);
-    if (!have || cost < best_cost) {
+    const int mis = warp_aligned(cand) ? 0 : 1;
+    if (!have || mis < best_mis || (mis == best_mis && cost < best_cost)) {
       have = true;
       best_cost = cost;
+      best_mis = mis;
       std::memcpy(best_t, cand, sizeof best_t);
     }
   };
@@ -787,6 +799,16 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
         }
         if (cc <= 1) break;
       }
+    }
+    // the largest power-of-two row count of the innermost outer dim that fits
+    if (r >= 2) {
+      int64_t tp[4] = {1, 1, 1, 1};
+      const int64_t lim = std::min<int64_t>(n[r - 2], D.cap_elems / widths[wi]);
+      int64_t pw = 1;
+      while (pw * 2 <= lim) pw *= 2;
+      tp[r - 2] = pw;
+      tp[r - 1] = widths[wi];
+      consider(tp);
     }
   }
   const int best = have ? 0 : -1;

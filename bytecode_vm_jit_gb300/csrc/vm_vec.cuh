@@ -41,8 +41,8 @@ constexpr int NW = kVmWarps;            // warps of the CTA
 constexpr int NCT = NW * 32;            // threads of the CTA
 constexpr int NTHREADS = NCT;
 constexpr int REG = kVmReg;             // fp32 values per FULL register per thread
-constexpr int kMaxRows = 64;            // rows per tile (a >= 128 elements, cap 8192)
-constexpr int kMaxSegs = 64;            // 512-byte segments per tile (8192 fp32 / 128)
+constexpr int kMaxRows = 128;           // rows per tile (a >= 128 elements, cap 16384)
+constexpr int kMaxSegs = 128;           // 512-byte segments per tile (16384 fp32 / 128)
 constexpr int kConsumerBar = 1;         // named barrier of the consumer warps
 // shared memory layout
 constexpr int kBarOff = kMaxImage;                        // 17 mbarriers (8 full, 8 empty, 1 hoist)
@@ -51,8 +51,9 @@ constexpr int kRowCoordOff = kRedOff + 2 * kMaxSegs * 4;  // outer coordinates o
 constexpr int kSegOff = kRowCoordOff + kMaxRows * 16;     // per segment: tile row << 16 | first column
 constexpr int kMiscOff = kSegOff + kMaxSegs * 4;          // grid-sum result, abort flag, CTA partials
 constexpr int kIssOff = kMiscOff + 128;                   // producer state (thread 0)
-constexpr int kRowSlotOff = kIssOff + 384;                // ROW values of ACC, slots 1, 2: [slot][warp][8]
-constexpr int kTmemOff = kRowSlotOff + 3 * NW * 8 * 4;    // TMEM base address (ROW areas: 8 values per warp)
+constexpr int kRowVals = kVmReg / 4;                      // ROW values a thread can hold (one per vector)
+constexpr int kRowSlotOff = kIssOff + 384;                // ROW values of ACC, slots 1, 2: [slot][warp][kRowVals]
+constexpr int kTmemOff = kRowSlotOff + 3 * NW * kRowVals * 4;  // TMEM base address
 constexpr int kUopOff = kTmemOff + 128;                   // decoded micro-ops of the current section
 constexpr int kDecOff = kUopOff + kMaxInstr * 16;         // words decoded one per lane (scratch)
 constexpr int kDataOff = kDecOff + kMaxInstr * 16;        // hoist area, then the stage ring
@@ -218,7 +219,7 @@ __device__ __forceinline__ void consumer_sync() { named_bar(kConsumerBar, NCT); 
 // ROW values are the same in every lane of a warp (the lanes share their segments), so
 // the ROW parts of ACC and the slots live in a small per-warp area of shared memory
 __device__ __forceinline__ float* rowslot(int k, int warp) {
-  return reinterpret_cast<float*>(dvm_smem + kRowSlotOff) + (k * NW + warp) * 8;
+  return reinterpret_cast<float*>(dvm_smem + kRowSlotOff) + (k * NW + warp) * kRowVals;
 }
 
 // =========================================================== DMA flow ==
@@ -545,12 +546,24 @@ __device__ __forceinline__ void tm_st16(uint32_t taddr, const float* v) {
 }
 // one FULL register (REG values) of this thread <-> TMEM
 __device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[REG]) {
-  if constexpr (REG == 32) tm_ld32w(taddr, v);
-  else tm_ld16(taddr, v);
+  if constexpr (REG == 64) {
+    tm_ld32w(taddr, v);
+    tm_ld32w(taddr + 32u, v + 32);
+  } else if constexpr (REG == 32) {
+    tm_ld32w(taddr, v);
+  } else {
+    tm_ld16(taddr, v);
+  }
 }
 __device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[REG]) {
-  if constexpr (REG == 32) tm_st32w(taddr, v);
-  else tm_st16(taddr, v);
+  if constexpr (REG == 64) {
+    tm_st32w(taddr, v);
+    tm_st32w(taddr + 32u, v + 32);
+  } else if constexpr (REG == 32) {
+    tm_st32w(taddr, v);
+  } else {
+    tm_st16(taddr, v);
+  }
 }
 __device__ __forceinline__ float4 tm_ld4(uint32_t taddr) {
   uint32_t a, b, c, d;

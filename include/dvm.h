@@ -95,7 +95,7 @@ typedef enum {
 /* description of the device the encoder plans for (see dvm_create_host) */
 typedef struct {
   int32_t num_cores;      /* CTAs per launch; default: SM count */
-  int32_t cap_elems;      /* padded elements per tile; default 8192 */
+  int32_t cap_elems;      /* padded elements per tile; default 16384 */
   int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 118784 */
   int32_t max_stages;     /* default 8 */
   int32_t c0_bytes;       /* per-tile overhead of the cost model; default 65536 */

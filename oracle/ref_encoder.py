@@ -53,7 +53,7 @@ MAGIC = 0x314D5644
 MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
 CUBE_RING_BYTES = 196608   # shared-memory ring of the MatMul tile op (A and W k-blocks)
 
-DEFAULT_DESC = dict(num_cores=152, cap_elems=8192, smem_budget=187392, max_stages=8,
+DEFAULT_DESC = dict(num_cores=152, cap_elems=16384, smem_budget=187392, max_stages=8,
                     c0_bytes=65536, flops_per_byte=280, n_slots=2)
 
 
@@ -67,6 +67,21 @@ def cdiv(a, b):
 
 def round_up(a, b):
     return cdiv(a, b) * b
+
+
+INTERP_WARPS = 8   # warps of the VEC interpreter that a tile's segments are dealt to
+
+
+def warp_aligned(t, r, a):
+    """Do the tile's rows map whole onto the interpreter's warps?  Segments (runs of
+    `a` elements of one row) are dealt to the warps in equal contiguous blocks; the plan
+    is aligned when the tile has one row or every block lies inside one row."""
+    rows = 1
+    for d in range(r - 1):
+        rows *= t[d]
+    m = t[r - 1] // a
+    nvu = cdiv(rows * m, INTERP_WARPS)
+    return rows == 1 or (m >= nvu and m % nvu == 0)
 
 
 def hardware_align_div(n, k, al):
@@ -757,6 +772,12 @@ class RefCtx:
                     if c <= 1:
                         break
                     k *= 2
+            # the largest power-of-two row count of the innermost outer dim that fits
+            if r >= 2:
+                p, lim = 1, min(G[r - 2], d_["cap_elems"] // w)
+                while p * 2 <= lim:
+                    p *= 2
+                cands.append([1] * (r - 2) + [p, w])
         best = None
         for cand in cands:
             rows = 1
@@ -781,8 +802,10 @@ class RefCtx:
                         cover *= cand[d]
                 tb += ESZ[ten["dtype"]] * cover
             cost = waves * (d_["c0_bytes"] + tb)
-            if best is None or cost < best[0]:
-                best = (cost, cand)
+            # plans whose rows map whole onto the interpreter's warps come first
+            key = (0 if warp_aligned(cand, r, a) else 1, cost)
+            if best is None or key < best[0]:
+                best = (key, cand)
         if best is None:
             raise EncodeError("capacity")
         t = best[1]
