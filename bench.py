@@ -589,32 +589,61 @@ def percentile(xs, q):
     return xs[k]
 
 
-def e2e_layernorm(wl, run, stream, sptr):
-    """Same metric through the C ABI with pinned host buffers: H2D of x, run, D2H of y."""
+def e2e_layernorm(wl, run, stream, sptr, n_copy=1):
+    """Same metric through the C ABI with pinned host buffers: H2D of x, run, D2H of y.
+
+    The transfers are pipelined against the kernels: each instance's x goes up on an
+    upload stream, the launch waits for it, and y comes back on a download stream once
+    its launch is done, so uploads, launches and downloads of neighbouring instances
+    overlap (one stream per direction measured fastest; `n_copy` splits each copy into
+    chunks on that many streams).  An upload into a pool region waits for the launch two
+    instances back (the rotating pools reuse a region only after several instances)."""
     import torch
     max_r = max(wl.sizes)
     hx = torch.empty(max_r * wl.d, dtype=torch.float32, pin_memory=True)
     hy = torch.empty(max_r * wl.d, dtype=torch.float32, pin_memory=True)
     hx.copy_(wl.pool_x[:max_r * wl.d].cpu())
+    up = [torch.cuda.Stream() for _ in range(n_copy)]
+    down = [torch.cuda.Stream() for _ in range(n_copy)]
+    insts = [wl.instance(i) for i in range(len(wl.sizes))]
     h2d = d2h = 0
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(len(wl.sizes)):
-        ops, ins, outs = wl.instance(i)
+    done = []
+    for i, (ops, ins, outs) in enumerate(insts):
         n = ins["x"].numel()
-        ins["x"].view(-1).copy_(hx[:n], non_blocking=True)
+        bounds = [n * c // n_copy for c in range(n_copy + 1)]
+        ups = []
+        for c, st in enumerate(up):
+            st.wait_event(e0)
+            if i >= 2:
+                st.wait_event(done[i - 2])
+            with torch.cuda.stream(st):
+                ins["x"].view(-1)[bounds[c]:bounds[c + 1]].copy_(hx[bounds[c]:bounds[c + 1]], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(st)
+                ups.append(ev)
+        for ev in ups:
+            stream.wait_event(ev)
         h2d += n * 4
         run.feed(ops, ins, outs, sptr)
-        hy[:n].copy_(outs["y"].view(-1), non_blocking=True)
+        k = torch.cuda.Event()
+        k.record(stream)
+        done.append(k)
+        for c, st in enumerate(down):
+            st.wait_event(k)
+            with torch.cuda.stream(st):
+                hy[bounds[c]:bounds[c + 1]].copy_(outs["y"].view(-1)[bounds[c]:bounds[c + 1]], non_blocking=True)
         d2h += n * 4
+    for st in down + up:
+        stream.wait_stream(st)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     return {"value": wl.unit_bytes() / (ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
-
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "copy_streams": n_copy}
 
 if __name__ == "__main__":
     main()
