@@ -141,6 +141,23 @@ def test_if_else_device_branch(i, t):
         assert np.array_equal(got, ref["t"]) or np.array_equal(got, ref["e"])
 
 
+def test_if_else_full_size_sampled_rows():
+    """T = 16384 (largest instance): the device branch follows the oracle's predicate over
+    all of x, and sampled rows of y equal the oracle's chosen branch, bit for bit."""
+    inp = W.if_else_inputs(7, 16384)
+    dev = to_dev(inp)
+    y = D.run_ops(W.IF_ELSE_ADD_OPS, dev, W.IF_ELSE_ADD_OUT)["y"]
+    torch.cuda.synchronize()
+    s_ref = evaluate(W.IF_ELSE_PRED_OPS, {"x": inp["x"]})["s"][0]
+    x = bf16_bits_to_f64(inp["x"][0])
+    assert abs(s_ref) > 2.0 ** -16 * np.sum(np.abs(x))       # the forced sign decides
+    rows = np.array([0, 1, 151, 152, 8191, 8192, 16382, 16383])
+    sample = {"x": (inp["x"][0][rows], "bf16"), "z": (inp["z"][0][rows], "bf16")}
+    branch = W.IF_ELSE_THEN_OPS if s_ref > 0 else W.IF_ELSE_ELSE_OPS
+    ref = evaluate(branch, sample)["y"]
+    assert np.array_equal(host(y[torch.from_numpy(rows).cuda()]), ref)
+
+
 def test_if_else_host_sync_variant_matches():
     inp = W.if_else_inputs(6, 500)
     dev = to_dev(inp)
@@ -179,6 +196,21 @@ def test_qwen_step(t):
     ref = evaluate(W.QWEN_STEP_OPS, inp)
     for k in W.QWEN_STEP_OUT:
         check_bf16(got[k], ref[k])
+
+
+def test_qwen_step_full_size_sampled_rows():
+    """T = 4096 (largest step): every op is row-wise, so sampled token rows of h, n and s
+    are checked against the oracle run on those rows alone."""
+    inp = W.qwen_inputs(4096, 4096)
+    dev = to_dev(inp)
+    out = D.run_ops(W.QWEN_STEP_OPS, dev, W.QWEN_STEP_OUT)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 151, 152, 2047, 2048, 4094, 4095])
+    sample = {k: ((a[rows] if a.ndim == 2 else a), dt) for k, (a, dt) in inp.items()}
+    ref = evaluate(W.QWEN_STEP_OPS, sample)
+    idx = torch.from_numpy(rows).cuda()
+    for k in W.QWEN_STEP_OUT:
+        check_bf16(host(out[k][idx]), ref[k])
 
 
 # ------------------------------------------------------------ op level -------
