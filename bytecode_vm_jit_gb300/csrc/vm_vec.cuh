@@ -462,7 +462,9 @@ __device__ __forceinline__ int ncol(const Prog& P, const TilePos& O, const Lanes
 // Each CTA allocates all 512 TMEM columns.  Warp w may access lanes 32*(w%4)..+31; the
 // NW/4 warps that share those lanes split the columns into blocks of kTmemPerThread.
 // In a thread's block, in units of one FULL register (REG columns): slot 1, slot 2,
-// the scratch register, a spare register, then kHoistCache hoisted-load cache registers.
+// the scratch register, a spare register, then kHoistCache dedicated registers.  The
+// spare, the dedicated ones and any slot the current section never touches cache
+// hoisted (tile-invariant) loads, so they are read from shared memory only once.
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTmemPerThread = 512 / (NW / 4);
 constexpr int kHoistCache = kTmemPerThread / REG - 4;
@@ -485,8 +487,7 @@ __device__ __forceinline__ uint32_t tm_base(uint32_t tmem) {
 }
 __device__ __forceinline__ uint32_t tm_slot(uint32_t tb, int k) { return tb + (uint32_t)((k - 1) * REG); }
 __device__ __forceinline__ uint32_t tm_scratch(uint32_t tb) { return tb + 2u * REG; }
-__device__ __forceinline__ uint32_t tm_spare(uint32_t tb) { return tb + 3u * REG; }
-__device__ __forceinline__ uint32_t tm_hoist(uint32_t tb, int k) { return tb + (uint32_t)((4 + k) * REG); }
+__device__ __forceinline__ uint32_t tm_reg(uint32_t tb, int r) { return tb + (uint32_t)(r * REG); }
 
 // 32 columns of this thread's lane <-> 32 registers; each access waits for its own
 // completion (the wait is in the same statement, so no use of the registers can be
@@ -967,7 +968,9 @@ __device__ __forceinline__ uint8_t light_handler(int op, int form, bool rev) {
 }
 
 // one word -> one micro-op (no fusion)
-__device__ __forceinline__ Uop decode_word(const Prog& P, const Instr* body, int i, int& hoisted) {
+// `cregs`: the registers that may cache hoisted loads, 4 bits each, `ncache` of them
+__device__ __forceinline__ Uop decode_word(const Prog& P, const Instr* body, int i, int& hoisted, uint32_t cregs,
+                                           int ncache) {
   const Instr w = body[i];
   Uop u;
   u.h = H_BAD;
@@ -992,9 +995,9 @@ __device__ __forceinline__ Uop decode_word(const Prog& P, const Instr* body, int
         u.h = esz == 4 ? H_LD_S4 : esz == 2 ? H_LD_S2 : H_LD_S1;
         if (w.flags & LF_HOIST) {
           u.off = kDataOff + P.pr->hoist_base + w.aux0;
-          if (hoisted < kHoistCache) {
+          if (hoisted < ncache) {
             u.h = H_LD_H;
-            u.aux = (uint8_t)(esz | (hoisted << 4));
+            u.aux = (uint8_t)(esz | (((cregs >> (4 * hoisted)) & 15u) << 4));
           }
           hoisted++;
         }
@@ -1070,6 +1073,26 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
   // (the row-reduction partials are free while a section is decoded)
   uint8_t* live = reinterpret_cast<uint8_t*>(red_buf(0));
   {
+    // FULL slots that the section names: the others may cache hoisted loads
+    bool use1 = false, use2 = false;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      uint32_t used = 0;
+      if (i < n) {
+        const Instr w = body[i];
+        if (w.op == OP_LD && !(w.flags & LF_ROWV)) used |= 1u << w.a;
+        if (w.op == OP_MOV && !(w.flags & 1)) used |= (1u << w.a) | (1u << w.b);
+        if (w.op >= OP_ADD && w.op <= OP_POW && !(w.flags & (CF_IMM | CF_XROW))) used |= 1u << w.a;
+      }
+      use1 = use1 || __any_sync(~0u, (used >> 1) & 1u);
+      use2 = use2 || __any_sync(~0u, (used >> 2) & 1u);
+    }
+    uint32_t cregs = 0;
+    int ncache = 0;
+    for (int k = 0; k < kHoistCache && ncache < 8; k++) cregs |= (uint32_t)(4 + k) << (4 * ncache++);
+    cregs |= 3u << (4 * ncache++);                      // the spare register
+    if (!use2) cregs |= 1u << (4 * ncache++);           // slot 2
+    if (!use1 && ncache < 8) cregs |= 0u << (4 * ncache++);  // slot 1
     // words in order, 32 at a time: the hoisted-load index of a word counts the hoisted
     // DMA loads before it
     int carry = 0;
@@ -1082,7 +1105,7 @@ __device__ __forceinline__ void decode_section(const Prog& P, const Instr* body,
       }
       const unsigned hm = __ballot_sync(~0u, hz);
       int hoisted = carry + __popc(hm & ((1u << lane) - 1u));
-      if (i < n) Ut[i] = decode_word(P, body, i, hoisted);
+      if (i < n) Ut[i] = decode_word(P, body, i, hoisted, cregs, ncache);
       carry += __popc(hm);
     }
     // liveness, last chunk first: the first later word that touches slot k decides
@@ -1414,7 +1437,7 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
           const uint8_t* region = ((u.fl & LF_HOIST) ? dvm_smem : stage_base) + u.off;
           const int k = u.aux >> 4;
           if (u.h == H_LD_H && (hmask & (1u << k))) {
-            tm_ld32(tm_hoist(tb, k), X);
+            tm_ld32(tm_reg(tb, k), X);
           } else {
             const int esz = u.h == H_LD_S4 ? 4 : u.h == H_LD_S2 ? 2 : u.h == H_LD_S1 ? 1 : (u.aux & 15);
             if (esz == 4) {
@@ -1425,7 +1448,7 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
               if constexpr (VE == 16) lds_vectors<VE, 1>(X, region, rs, L);
             }
             if (u.h == H_LD_H) {
-              tm_st32(tm_hoist(tb, k), X);
+              tm_st32(tm_reg(tb, k), X);
               hmask |= 1u << k;
             }
           }
@@ -1628,8 +1651,7 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         uint32_t xcol = 0;
         if (!xr && !imm) {
           if (u.a == 0) {
-            tm_st32(tm_spare(tb), A);  // X = ACC itself: a copy in the spare register
-            xcol = tm_spare(tb);
+            xcol = tm_scratch(tb);  // X = ACC itself: the loop reads both operands of an element before writing it
           } else {
             xcol = tm_slot(tb, u.a);
           }
