@@ -83,6 +83,55 @@ def test_header_counts_and_tile_alignment(shape):
     assert p["n"][:r] == list(shape)
 
 
+def _plan(ops, inputs, outs):
+    spec = {k: (dt, s, None) for k, (dt, s) in inputs.items()}
+    _, _, launches = R.replay(ops, spec, outs)
+    return [(p["t"][:p["rank"]], p["rank"], parse(img)[0]["ve"]) for img, _ in launches for p in parse(img)[1]]
+
+
+def _aligned(t, r, ve):
+    """Independent restatement of the warp-alignment rule: deal the tile's segments
+    (runs of 32*ve elements of one row) to 8 warps in equal contiguous blocks; every
+    block must lie inside one row."""
+    a = 32 * ve
+    rows = int(np.prod(t[:r - 1])) if r > 1 else 1
+    m = t[r - 1] // a
+    segs = rows * m
+    per = -(-segs // 8)
+    blocks = [(w * per, min(segs, (w + 1) * per)) for w in range(8) if w * per < segs]
+    return all(lo // m == (hi - 1) // m for lo, hi in blocks)
+
+
+@pytest.mark.parametrize("rows", [1, 3, 37, 1000, 16896, 65536])
+def test_layernorm_plans_are_warp_aligned(rows):
+    (t, r, ve), = _plan(W.LAYERNORM_OPS, {"x": ("f32", (rows, 4096)), "gamma": ("f32", (4096,)),
+                                          "beta": ("f32", (4096,))}, W.LAYERNORM_OUT)
+    assert _aligned(t, r, ve)
+    if rows >= 4 * R.DEFAULT_DESC["num_cores"]:
+        # more than a wave of tiles: the power-of-two row candidate, 4 rows of 4096, fills
+        # the 16384-element capacity (below that, one-row tiles cost fewer bytes per wave)
+        assert t == [4, 4096]
+
+
+def test_benchmark_shapes_get_full_aligned_tiles():
+    assert _plan(W.SQRT_ADD_OPS, {"a": ("f32", (4096, 1024)), "b": ("f32", (4096, 1024))},
+                 W.SQRT_ADD_OUT)[0][0] == [8, 1024]
+    assert _plan(W.IF_ELSE_ADD_OPS, {"x": ("bf16", (5000, 8192)), "z": ("bf16", (5000, 8192))},
+                 W.IF_ELSE_ADD_OUT)[0][0] == [2, 8192]
+    for t, r, ve in _plan(W.QWEN_STEP_OPS, {"x": ("bf16", (1000, 5120)), "r": ("bf16", (1000, 5120)),
+                                            "w": ("bf16", (5120,)), "g": ("bf16", (1000, 17408)),
+                                            "u": ("bf16", (1000, 17408))}, W.QWEN_STEP_OUT):
+        assert _aligned(t, r, ve)
+
+
+@pytest.mark.parametrize("shape", [(3, 4096), (5, 1000), (63, 256), (7, 129), (300, 8192), (2, 3, 384)])
+def test_plans_are_aligned_when_an_aligned_plan_exists(shape):
+    """A one-row tile is always aligned, so every element-wise plan must be."""
+    spec = {"a": ("f32", shape), "b": ("f32", shape)}
+    for t, r, ve in _plan(W.SQRT_ADD_OPS, spec, W.SQRT_ADD_OUT):
+        assert _aligned(t, r, ve)
+
+
 def _counts(ops, inputs, outs, strides=None):
     spec = {k: (dt, s, (strides or {}).get(k)) for k, (dt, s) in inputs.items()}
     ctx, _, launches = R.replay(ops, spec, outs)
