@@ -3,9 +3,10 @@
 //
 // Execution model (DVM review page, section 4.4 "virtual machine execution"): each CTA
 // is one "AI core"; it computes its contiguous tile range [c*body_tile,
-// min((c+1)*body_tile, block_dim)) and, for each tile, decodes the code body and runs
-// the matching virtual-instruction function.  Decoding is warp-uniform from the image
-// staged in shared memory.  Section 3.2's asynchronous flows map onto one CTA:
+// min((c+1)*body_tile, block_dim)) and, for each tile, runs the virtual-instruction
+// functions of the code body.  The body, staged in shared memory with the image, is
+// decoded once per program (or section) by warp 1 into micro-ops; every tile then
+// dispatches on them warp-uniformly.  Section 3.2's asynchronous flows map onto one CTA:
 //   * DMA flow    -> thread 0 keeps a ring of shared-memory stages filled ahead with
 //                    cp.async.bulk copies, completion counted on mbarriers; it tops the
 //                    ring up without blocking and waits only when the ring runs dry;
@@ -14,17 +15,17 @@
 //                    shuffles, and store from registers straight to HBM (ST);
 //   * the WAIT / REL words the encoder inserts are the syncs between the two flows.
 //
-// Registers follow an accumulator machine: ACC (32 fp32 values per thread) lives in
+// Registers follow an accumulator machine: ACC (64 fp32 values per thread) lives in
 // registers; the two addressable slots live in tensor memory (TMEM), which this kernel
-// uses as an extension of the register file: tcgen05.st / tcgen05.ld move a whole
-// 32-value register of a thread in one instruction, without touching shared memory.
+// uses as an extension of the register file: tcgen05.st / tcgen05.ld move 32 values of
+// a thread's register per instruction, without touching shared memory.
 // An instruction with a slot operand loads it into one temporary register array, so
 // every opcode has exactly one code path and the interpreter stays small enough for
 // the instruction caches.  A ROW value (one number per tile row: a row sum, mean or
 // rstd) is the same in every lane of a warp and lives in a small per-warp area of
 // shared memory; in programs where all of a thread's vectors lie in one tile row it is
 // computed once.  A row reduction costs a warp butterfly, one partial per warp in
-// shared memory and one CTA barrier.
+// shared memory and a named barrier of the warps that hold the row.
 //
 // Grid-wide sums (if-else-add's predicate) end a section with a bounded grid barrier in
 // a cooperative launch; the branch is then taken on the device (JLE0), no host
@@ -214,7 +215,6 @@ __device__ __forceinline__ float* red_buf(int b) { return reinterpret_cast<float
 __device__ __forceinline__ float* misc_scalar() { return reinterpret_cast<float*>(dvm_smem + kMiscOff); }
 __device__ __forceinline__ volatile int* abort_flag() { return reinterpret_cast<volatile int*>(dvm_smem + kMiscOff + 16); }
 __device__ __forceinline__ float* cta_partials() { return reinterpret_cast<float*>(dvm_smem + kMiscOff + 64); }
-__device__ __forceinline__ uint8_t* hoist_area() { return dvm_smem + kDataOff; }
 __device__ __forceinline__ void consumer_sync() { named_bar(kConsumerBar, NCT); }
 // ROW values are the same in every lane of a warp (the lanes share their segments), so
 // the ROW parts of ACC and the slots live in a small per-warp area of shared memory
