@@ -16,6 +16,7 @@ Algorithmic bytes per instance (what a perfect fused kernel must move):
   if_else_add 65536*T (predicate pass reads x, branch pass reads x, z, writes y)
   qwen_stream 145408*T + 10240
   matmul      2*M*4096*4096 flops (reported in TFLOP/s); bytes 16384*M + 33554432 + 8192
+  addmm       2*M*4096*4096 flops (TFLOP/s); bytes 32768*M + 33554432 (A, C read, y written, W)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -156,6 +157,13 @@ class Workload:
             self.pool_y = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
             self.pool_n = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
             self.pool_s = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+        elif name == "addmm":
+            self.sizes = W.matmul_rows()
+            wt, _, _ = W.matmul_params()
+            self.wt = W.bf16_bits_to_torch(wt).to(dev)
+            self.pool_x = W.device_pool(4 << 30, "bf16", "normal", 103 + seed_off, dev, std=0.02)
+            self.pool_c = W.device_pool(1 << 30, "bf16", "normal", 303 + seed_off, dev, std=0.1)
+            self.pool_y = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
         elif name == "matmul":
             self.sizes = W.matmul_rows()
             wt, bias, _ = W.matmul_params()
@@ -185,10 +193,12 @@ class Workload:
             return 65536 * size
         if self.name == "matmul":
             return 16384 * size + 33554432 + 8192
+        if self.name == "addmm":
+            return 32768 * size + 33554432
         return 145408 * size + 10240
 
     def flops_of(self, size):
-        return 2 * size * self.W.MM_N * self.W.MM_K if self.name == "matmul" else 0
+        return 2 * size * self.W.MM_N * self.W.MM_K if self.name in ("matmul", "addmm") else 0
 
     def unit_bytes(self):
         return sum(self.bytes_of(s) for s in self.sizes)
@@ -211,6 +221,11 @@ class Workload:
             z = self.take(self.pool_z, s * self.d, (s, self.d))
             y = self.take(self.pool_y, s * self.d, (s, self.d))
             return W.IF_ELSE_ADD_OPS, {"x": x, "z": z}, {"y": y}
+        if self.name == "addmm":
+            a = self.take(self.pool_x, s * W.MM_K, (s, W.MM_K))
+            c = self.take(self.pool_c, s * W.MM_N, (s, W.MM_N))
+            y = self.take(self.pool_y, s * W.MM_N, (s, W.MM_N))
+            return W.ADDMM_OPS, {"A": a, "W": self.wt.t(), "C": c}, {"y": y}
         if self.name == "matmul":
             a = self.take(self.pool_x, s * W.MM_K, (s, W.MM_K))
             y = self.take(self.pool_y, s * W.MM_N, (s, W.MM_N))
@@ -324,15 +339,20 @@ def cpu_baseline(name, budget_s=15.0):
             if t_sum > budget_s:
                 break
         sample = "first %d of the 500 if-else-add instances" % done
-    elif name == "matmul":
+    elif name in ("matmul", "addmm"):
         sizes = W.matmul_rows()
         wt, bias, _ = W.matmul_params()
         f_sum = 0
         for i, m in enumerate(sizes):
             inp = W.matmul_inputs(i, m, small_params=(wt, bias))
-            inp = {"A": inp["A"], "W": (np.ascontiguousarray(wt.T), "bf16"), "bias": inp["bias"]}
+            if name == "matmul":
+                ops = W.MATMUL_ABS_OPS
+                inp = {"A": inp["A"], "W": (np.ascontiguousarray(wt.T), "bf16"), "bias": inp["bias"]}
+            else:
+                ops = W.ADDMM_OPS
+                inp = {"A": inp["A"], "W": (np.ascontiguousarray(wt.T), "bf16"), "C": (W.addmm_c(i, m), "bf16")}
             t0 = time.perf_counter()
-            evaluate(W.MATMUL_ABS_OPS, inp)
+            evaluate(ops, inp)
             t_sum += time.perf_counter() - t0
             f_sum += 2 * m * W.MM_N * W.MM_K
             done += 1
@@ -340,8 +360,8 @@ def cpu_baseline(name, budget_s=15.0):
                 break
         cores = int(os.environ.get("OMP_NUM_THREADS", "1"))
         return {"value": f_sum / t_sum / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                "sample": "first %d of the 100 MatMul+Abs instances (M %d..%d), fp64 numpy matmul" % (
-                    done, min(sizes[:done]), max(sizes[:done])),
+                "sample": "first %d of the 100 %s instances (M %d..%d), fp64 numpy matmul" % (
+                    done, "MatMul+Abs" if name == "matmul" else "addmm", min(sizes[:done]), max(sizes[:done])),
                 "seconds": round(t_sum, 3), "instances": done}
     else:
         sizes = W.qwen_tokens()
@@ -387,7 +407,7 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dvm", choices=["dvm", "reference"])
-    ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream", "matmul"])
+    ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream", "matmul", "addmm"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--instances", type=int, default=0, help="use only the first N instances (profiling)")
     ap.add_argument("--fixed-size", type=int, default=0, help="override every instance's size (profiling)")
@@ -407,8 +427,10 @@ def main():
         "qwen_stream": "Qwen3-14B-shaped stream (h=x+r, RMSNorm, silu(g)*u), first 200 of 2000 steps",
         "matmul": "y = Abs(A@W + bias)*0.5, bf16 in / fp32 acc / bf16 out, A[M,4096], W[4096,4096], "
                   "M log-uniform in [1,8192], 100 instances (seed 3)",
+        "addmm": "y = 2*C + 0.5*(A@W), bf16 in / fp32 acc / bf16 out, A[M,4096], W[4096,4096], C[M,4096], "
+                 "M log-uniform in [1,8192], 100 instances (seed 3)",
     }[args.config]
-    is_mm = args.config == "matmul"
+    is_mm = args.config in ("matmul", "addmm")
     metric = METRIC_MM if is_mm else METRIC
     unit = "TFLOP/s" if is_mm else "GB/s"
 
@@ -505,7 +527,8 @@ def main():
     kernel_gbs = wl.unit_bytes() / (kernel_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
     key = {"layernorm": "vm_vec_kernel<4>", "sqrt_add": "vm_vec_kernel<4>", "if_else_add": "vm_vec_kernel<8>",
-           "qwen_stream": "vm_vec_kernel<8>", "matmul": "vm_cube_kernel"}[args.config]
+           "qwen_stream": "vm_vec_kernel<8>", "matmul": "vm_cube_kernel",
+           "addmm": "vm_cube_kernel"}[args.config]
     traffic_per_unit, _ = roofline_traffic(key + ":" + args.config)
     traffic = None
     if traffic_per_unit is not None:

@@ -80,6 +80,19 @@ MATMUL_ABS_OPS = [
 ]
 MATMUL_ABS_OUT = ["y"]
 
+# addmm (the review's Table 3 op): y = beta * C + alpha * (A @ W), C a full [M, N]
+# operand read by the epilogue; and the MatMul tile op alone (bf16 result)
+ADDMM_ALPHA, ADDMM_BETA = 0.5, 2.0
+ADDMM_OPS = [
+    ("matmul", ["A", "W"], "p", "f32", ()),
+    ("muls", ["p"], "q", "f32", (ADDMM_ALPHA, 0)),
+    ("muls", ["C"], "c2", "f32", (ADDMM_BETA, 0)),
+    ("add", ["q", "c2"], "y", "bf16", ()),
+]
+ADDMM_OUT = ["y"]
+MATMUL_OPS = [("matmul", ["A", "W"], "y", "bf16", ())]
+MATMUL_OUT = ["y"]
+
 RMS_EPS = 1e-6
 QWEN_STEP_OPS = [
     ("add", ["x", "r"], "h", "bf16", ()),
@@ -203,6 +216,12 @@ def matmul_inputs(i, m, seed=3, k=MM_K, n=MM_N, small_params=None):
     rng = np.random.default_rng([seed, i])
     a = f32_to_bf16_bits(_normal_f32(rng, (m, k), 0.0, 0.02))
     return {"A": (a, "bf16"), "Wt": (wt, "bf16"), "bias": (bias, "bf16")}
+
+
+def addmm_c(i, m, seed=5, n=MM_N):
+    """C [m, n] bf16 ~ N(0, 0.1) for instance i."""
+    rng = np.random.default_rng([seed, i])
+    return f32_to_bf16_bits(_normal_f32(rng, (m, n), 0.0, 0.1))
 
 
 # qwen_stream -----------------------------------------------------------------

@@ -178,6 +178,50 @@ def test_matmul_epilogue_full_and_row_operands_fp32_out():
     assert err.max() <= 1e-3, err.max()
 
 
+# ------------------------------------------- addmm and the MatMul op alone --
+def _run_one_cube_launch(ops, inputs, outs):
+    ctx = D.Ctx(0)
+    try:
+        out = ctx.feed(ops, inputs, outs)
+        assert ctx.poll() == 0
+        kinds = [img[6] for img, _ in ctx.launch_log]
+    finally:
+        ctx.close()
+    torch.cuda.synchronize()
+    assert kinds == [2], "expected one CUBE launch, got kernel types %r" % kinds
+    return {k: host(v) for k, v in out.items()}
+
+
+@pytest.mark.parametrize("m", [1, 129, 300, 2048])
+def test_addmm(m):
+    """y = 2 * C + 0.5 * (A @ W): the beta-scaled full operand C is read by the epilogue."""
+    wt, _, _ = W.matmul_params()
+    inp = W.matmul_inputs(m, m, small_params=(wt, np.zeros(W.MM_N, np.uint16)))
+    c = W.addmm_c(m, m)
+    got = _run_one_cube_launch(W.ADDMM_OPS, {"A": dev_bf16(inp["A"][0]), "W": dev_bf16(wt).t(), "C": dev_bf16(c)},
+                               W.ADDMM_OUT)["y"]
+    ref = evaluate(W.ADDMM_OPS, {"A": inp["A"], "W": (np.ascontiguousarray(wt.T), "bf16"), "C": (c, "bf16")})["y"]
+    check_bf16(got, ref)
+
+
+@pytest.mark.parametrize("m,out_dt", [(1, "bf16"), (300, "bf16"), (129, "f32"), (1000, "f32")])
+def test_matmul_alone(m, out_dt):
+    wt, _, _ = W.matmul_params()
+    inp = W.matmul_inputs(m + 1000, m, small_params=(wt, np.zeros(W.MM_N, np.uint16)))
+    ops = [("matmul", ["A", "W"], "y", out_dt, ())]
+    got = _run_one_cube_launch(ops, {"A": dev_bf16(inp["A"][0]), "W": dev_bf16(wt).t()}, ["y"])["y"]
+    ref = evaluate(ops, {"A": inp["A"], "W": (np.ascontiguousarray(wt.T), "bf16")})["y"]
+    if out_dt == "bf16":
+        check_bf16(got, ref)
+    else:
+        # fp32 accumulation of K = 4096 exact bf16 products: the standard bound
+        # gamma_K * sum_k |a_k w_k|, gamma_K = K u / (1 - K u), u = 2^-24
+        a, w = bf16_bits_to_f64(inp["A"][0]), bf16_bits_to_f64(wt)
+        k = a.shape[1]
+        gamma = k * 2.0 ** -24 / (1 - k * 2.0 ** -24)
+        assert np.all(np.abs(got - ref) <= gamma * (np.abs(a) @ np.abs(w).T) + 1e-30)
+
+
 def test_matmul_dynamic_instances_sampled_rows():
     """Ten instances of the dynamic-M stream, each encoded as a new shape: 8 sampled
     rows per instance against the oracle."""
