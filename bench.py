@@ -248,6 +248,7 @@ class Runner:
         self.D = D
         self.h = D.dvm_create(dev_index)
         self.launches = 0
+        self.batches = {}        # op list -> its packed dvm_graph_add_n stream
         self.encode_ns = []      # in-library host time per instance
         self.wall_ns = []        # Python-side host time per instance (graph_add..run)
 
@@ -256,21 +257,20 @@ class Runner:
         h = self.h
         t0 = time.perf_counter_ns()
         D.dvm_reset(h)
-        ids, tens = {}, {}
+        # the op list goes in with one dvm_graph_add_n call per part (packed once); a part
+        # that ends with an opaque op is flushed and run before the next one
+        key = (id(ops), tuple(inputs), tuple(outputs))
+        batch = self.batches.get(key)
+        if batch is None:
+            batch = self.batches[key] = D.OpBatch(ops, list(inputs), set(outputs))
+        tens = {}
         for name, t in inputs.items():
-            vid = D.dvm_input(h, D._dt_name(t), list(t.shape), list(t.stride()))
-            ids[name] = vid
-            tens[vid] = t
-        for op, ins, out, dt, attrs in ops:
-            if op == "opaque":
-                D.dvm_graph_add(h, "opaque", [], dt)
+            tens[D.dvm_input(h, D._dt_name(t), list(t.shape), list(t.stride()))] = t
+        for name, t in outputs.items():
+            tens[batch.ids[name]] = t
+        for k in range(len(batch.packed)):
+            if batch.add(h, k):
                 self._run_pending(tens, stream, events)
-                continue
-            vid = D.dvm_graph_add(h, op, [ids[i] for i in ins], dt, attrs)
-            ids[out] = vid
-            if out in outputs:
-                D.dvm_mark_output(h, vid)
-                tens[vid] = outputs[out]
         self._run_pending(tens, stream, events)
         self.encode_ns.append(D.dvm_stats(h)["host_ns_last"])
         self.wall_ns.append(time.perf_counter_ns() - t0)

@@ -29,7 +29,7 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_OP", -3: "SHAPE", -4: "BU
 EXPORTS = ["dvm_create", "dvm_create_host", "dvm_destroy", "dvm_reset", "dvm_get_desc", "dvm_input",
            "dvm_graph_add", "dvm_mark_output", "dvm_value_info", "dvm_flush", "dvm_encode",
            "dvm_validate", "dvm_run", "dvm_poll_status", "dvm_last_error", "dvm_stats",
-           "dvm_stats_reset_last", "dvm_debug_set_barrier", "dvm_run_static"]
+           "dvm_stats_reset_last", "dvm_debug_set_barrier", "dvm_run_static", "dvm_graph_add_n"]
 
 MAX_IMAGE = 8192
 MAX_BIND = 16
@@ -44,6 +44,13 @@ class DvmError(RuntimeError):
 class DeviceDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("num_cores", "cap_elems", "smem_budget", "max_stages",
                                               "c0_bytes", "flops_per_byte", "n_slots")]
+
+
+class OpDesc(ctypes.Structure):
+    """One op of dvm_graph_add_n (the arguments of one dvm_graph_add call)."""
+    _fields_ = [("op", ctypes.c_int32), ("n_inputs", ctypes.c_int32), ("inputs", ctypes.c_int32 * 4),
+                ("rank", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("shape", ctypes.c_int64 * 4),
+                ("n_attrs", ctypes.c_int32), ("attrs", ctypes.c_float * 4), ("mark_output", ctypes.c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -85,6 +92,7 @@ def lib():
     L.dvm_stats_reset_last.argtypes = [VP]
     L.dvm_debug_set_barrier.argtypes = [VP, ctypes.c_int, ctypes.c_int]
     L.dvm_run_static.argtypes = [ctypes.c_char_p, ctypes.c_size_t, P(VP), ctypes.c_int, VP]
+    L.dvm_graph_add_n.argtypes = [VP, P(OpDesc), ctypes.c_int, P(I32)]
     for n in EXPORTS:
         f = getattr(L, n)
         if n not in ("dvm_destroy", "dvm_last_error"):
@@ -177,6 +185,67 @@ def dvm_graph_add(ctx, op, inputs, dtype, attrs=(), shape=None):
     _check(ctx, lib().dvm_graph_add(ctx, OPS[op], ins, len(inputs), sh, rank, DTYPES[dtype], at, len(attrs),
                                      S.out_ref))
     return S.out.value
+
+
+def dvm_graph_add_n(ctx, descs, out_ids):
+    """Append a packed op stream (ctypes array of OpDesc); out_ids receives the ids."""
+    _check(ctx, lib().dvm_graph_add_n(ctx, descs, len(descs), out_ids))
+
+
+class OpBatch:
+    """An op stream (tuples (op, input_names, out_name, out_dtype, attrs)) packed once for
+    dvm_graph_add_n.  After dvm_reset, value ids are handed out in order: the inputs
+    declared in `input_names` order take 0..k-1 and every op with a result the next id,
+    so the ids that later ops read are known when the stream is packed.  An opaque op
+    ends a part (it is the part's last op): the caller flushes and runs the launches
+    after such a part, as after a dvm_graph_add of that op."""
+
+    def __init__(self, ops, input_names, outputs):
+        ids = {name: i for i, name in enumerate(input_names)}
+        nxt = len(input_names)
+        self.parts = []
+        cur = []
+        for op in ops:
+            cur.append(op)
+            if op[0] == "opaque":
+                self.parts.append(cur)
+                cur = []
+        if cur:
+            self.parts.append(cur)
+        self.packed = []
+        for part in self.parts:
+            descs = (OpDesc * len(part))()
+            expect = []
+            for j, (op, ins, out, dt, attrs) in enumerate(part):
+                d = descs[j]
+                d.op = OPS[op]
+                d.n_inputs = len(ins)
+                for q, name in enumerate(ins):
+                    d.inputs[q] = ids[name]
+                d.out_dtype = DTYPES[dt]
+                d.n_attrs = len(attrs)
+                for q, a in enumerate(attrs):
+                    d.attrs[q] = a
+                if op == "opaque":
+                    d.rank = 0
+                    expect.append(-1)
+                    continue
+                d.rank = -1
+                d.mark_output = 1 if out in outputs else 0
+                ids[out] = nxt
+                expect.append(nxt)
+                nxt += 1
+            self.packed.append((descs, expect, (ctypes.c_int32 * len(part))(), part[-1][0] == "opaque"))
+        self.ids = ids
+
+    def add(self, ctx, part):
+        """Append part `part` to ctx (reset, inputs declared in order, earlier parts added).
+        Returns True when the part ends with an opaque op (flush and run now)."""
+        descs, expect, out_ids, opaque = self.packed[part]
+        dvm_graph_add_n(ctx, descs, out_ids)
+        if list(out_ids) != expect:
+            raise RuntimeError("value ids differ from the packed stream's (inputs not declared first?)")
+        return opaque
 
 
 def dvm_mark_output(ctx, vid):
@@ -290,6 +359,7 @@ class Ctx:
         self.tensors = {}     # value id -> torch tensor
         self.ids = {}         # name -> value id
         self.launch_log = []  # (image, binding ids) of every launch run
+        self.batches = {}     # op list -> its packed dvm_graph_add_n stream
 
     def close(self):
         if self.h:
@@ -340,8 +410,21 @@ class Ctx:
         return n
 
     def feed(self, ops, inputs, outputs, stream=None):
+        fresh = not self.ids and not self.tensors
         for name, t in inputs.items():
             self.bind_input(name, t)
+        if fresh:
+            # a fresh context: the stream goes in with one dvm_graph_add_n call per part
+            key = (id(ops), tuple(inputs), tuple(outputs))
+            batch = self.batches.get(key)
+            if batch is None:
+                batch = self.batches[key] = OpBatch(ops, list(inputs), set(outputs))
+            for k in range(len(batch.packed)):
+                if batch.add(self.h, k):
+                    self.run_pending(stream)
+            self.ids.update(batch.ids)
+            self.run_pending(stream)
+            return {name: self.tensors[self.ids[name]] for name in outputs}
         for op, ins, out, dt, attrs in ops:
             if op == "opaque":
                 dvm_graph_add(self.h, "opaque", [], dt)

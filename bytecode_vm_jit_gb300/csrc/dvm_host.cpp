@@ -1381,6 +1381,25 @@ dvm_status dvm_graph_add(dvm_ctx* c, dvm_op opc, const int32_t* inputs, int n_in
   return DVM_OK;
 }
 
+dvm_status dvm_graph_add_n(dvm_ctx* c, const dvm_op_desc* ops, int n, int32_t* out_ids) {
+  if (!c || n < 0 || (n > 0 && (!ops || !out_ids))) return DVM_E_INVALID_ARG;
+  for (int i = 0; i < n; i++) {
+    const dvm_op_desc& d = ops[i];
+    if (d.n_inputs < 0 || d.n_inputs > 4 || d.n_attrs < 0 || d.n_attrs > 4 || d.rank < -1 || d.rank > 4)
+      return c->fail(DVM_E_INVALID_ARG, "dvm_graph_add_n: bad input, attribute or rank count");
+    int32_t id = -1;
+    dvm_status rc = dvm_graph_add(c, (dvm_op)d.op, d.inputs, d.n_inputs, d.rank > 0 ? d.shape : nullptr, d.rank,
+                                  (dvm_dtype)d.out_dtype, d.attrs, d.n_attrs, &id);
+    if (rc != DVM_OK) return rc;
+    out_ids[i] = id;
+    if (d.mark_output && id >= 0) {
+      rc = dvm_mark_output(c, id);
+      if (rc != DVM_OK) return rc;
+    }
+  }
+  return DVM_OK;
+}
+
 dvm_status dvm_mark_output(dvm_ctx* c, int32_t id) {
   if (!c || id < 0 || id >= (int32_t)c->values.size()) return DVM_E_INVALID_ARG;
   c->values[id].output = true;

@@ -96,7 +96,7 @@ typedef enum {
 typedef struct {
   int32_t num_cores;      /* CTAs per launch; default: SM count */
   int32_t cap_elems;      /* padded elements per tile; default 16384 */
-  int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 118784 */
+  int32_t smem_budget;    /* bytes for the DMA ring plus hoist area; default 187392 */
   int32_t max_stages;     /* default 8 */
   int32_t c0_bytes;       /* per-tile overhead of the cost model; default 65536 */
   int32_t flops_per_byte; /* cube cost-model balance; default 280 */
@@ -141,6 +141,25 @@ dvm_status dvm_graph_add(dvm_ctx* ctx, dvm_op op, const int32_t* inputs, int n_i
 /* Ask that value `id` be written to memory (otherwise a fused intermediate lives only
  * in registers unless an op of another group reads it). */
 dvm_status dvm_mark_output(dvm_ctx* ctx, int32_t id);
+
+/* One op of dvm_graph_add_n: the arguments of one dvm_graph_add call. */
+typedef struct {
+  int32_t op;           /* dvm_op */
+  int32_t n_inputs;     /* 0..4 */
+  int32_t inputs[4];    /* value ids */
+  int32_t rank;         /* result rank; -1 = infer it (as dvm_graph_add with shape NULL) */
+  int32_t out_dtype;    /* dvm_dtype */
+  int64_t shape[4];     /* result shape when rank > 0 */
+  int32_t n_attrs;      /* 0..4 */
+  float attrs[4];
+  int32_t mark_output;  /* nonzero: also dvm_mark_output on the result */
+} dvm_op_desc;
+/* Append n ops in order, as n calls of dvm_graph_add (each followed by dvm_mark_output
+ * where its desc asks): one call per op stream instead of one per op, for callers whose
+ * per-call overhead is high.  out_ids[i] (n entries, caller-owned) = the result id of op
+ * i.  On an error the ops before the failing one stay appended, that op's status is
+ * returned and the out_ids of it and of later ops are not written. */
+dvm_status dvm_graph_add_n(dvm_ctx* ctx, const dvm_op_desc* ops, int n, int32_t* out_ids);
 /* Query a value: dtype, rank, shape[4]. */
 dvm_status dvm_value_info(const dvm_ctx* ctx, int32_t id, int32_t* dtype, int32_t* rank,
                           int64_t* shape);

@@ -250,3 +250,37 @@ def test_encode_latency_is_microseconds():
         assert np.median(per) < 200.0     # generous on a loaded CI box; bench reports the real number
     finally:
         D.dvm_destroy(ctx)
+
+
+@pytest.mark.parametrize("name", ["layernorm", "sqrt_add", "if_else_add", "qwen", "matmul_abs"])
+def test_graph_add_n_matches_op_by_op(name):
+    """One dvm_graph_add_n call per op stream gives the same launch images as one
+    dvm_graph_add call per op."""
+    cases = {
+        "layernorm": (W.LAYERNORM_OPS, {"x": ("f32", (1000, 4096), None), "gamma": ("f32", (4096,), None),
+                                        "beta": ("f32", (4096,), None)}, W.LAYERNORM_OUT),
+        "sqrt_add": (W.SQRT_ADD_OPS, {"a": ("f32", (333, 1024), None), "b": ("f32", (333, 1024), None)},
+                     W.SQRT_ADD_OUT),
+        "if_else_add": (W.IF_ELSE_ADD_OPS, {"x": ("bf16", (300, 8192), None), "z": ("bf16", (300, 8192), None)},
+                        W.IF_ELSE_ADD_OUT),
+        "qwen": (W.QWEN_STEP_OPS, {"x": ("bf16", (200, 5120), None), "r": ("bf16", (200, 5120), None),
+                                   "w": ("bf16", (5120,), None), "g": ("bf16", (200, 17408), None),
+                                   "u": ("bf16", (200, 17408), None)}, W.QWEN_STEP_OUT),
+        "matmul_abs": (W.MATMUL_ABS_OPS, {"A": ("bf16", (77, 4096), None), "W": ("bf16", (4096, 4096), [1, 4096]),
+                                          "bias": ("bf16", (4096,), None)}, W.MATMUL_ABS_OUT),
+    }
+    ops, inputs, outs = cases[name]
+    ref = cxx_replay(ops, inputs, outs)
+    ctx = D.dvm_create_host()
+    try:
+        for nm, (dt, shape, strides) in inputs.items():
+            D.dvm_input(ctx, dt, list(shape), strides)
+        batch = D.OpBatch(ops, list(inputs), set(outs))
+        got = []
+        for k in range(len(batch.packed)):
+            batch.add(ctx, k)
+            n = D.dvm_flush(ctx)      # after an opaque op, and at the end
+            got += [D.dvm_encode(ctx, i)[0] for i in range(n)]
+    finally:
+        D.dvm_destroy(ctx)
+    assert got == [img for img, _ in ref]
