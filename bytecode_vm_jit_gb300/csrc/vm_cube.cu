@@ -46,7 +46,7 @@ constexpr int kBK = 64;    // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kUK = 16;    // K of one tcgen05.mma.kind::f16
 
 struct CubeParams {
-  CUtensorMap tmA;         // A [M, K], box {64, 128}
+  CUtensorMap tmA;         // A [M, K], box {64, min(128, M rounded up to 8)}
   CUtensorMap tmW;         // W as [N, K] (K contiguous), box {64, t_N}
   alignas(16) uint8_t image[kMaxImage];
   void* ptrs[kMaxBind];
@@ -582,6 +582,10 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
   const int M = (int)pr->n[0], N = (int)pr->n[1], K = (int)pr->K;
   const int BN = (int)pr->t[1];
   const int tiles_n = (N + BN - 1) / BN;
+  // A's TMA box is min(128, M rounded up to 8) rows: an instance with fewer than 128 rows
+  // copies only those (the rows of the A tile beyond them feed accumulator rows that the
+  // epilogue never stores)
+  const uint32_t a_box_bytes = (uint32_t)min(kBM, (M + 7) & ~7) * kBK * 2;
   const int nkb = (K + kBK - 1) / kBK;
   // two accumulators of BN columns, each starting on a multiple of 32 columns so that
   // the epilogue's 32-column reads stay inside the accumulator they belong to
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
           const int s = it % S;
           const uint32_t ph = (uint32_t)(it / S) & 1u;
           if (!mbar_spin(&C->empty[s], ph ^ 1u, st, abort)) break;
-          mbar_arrive_expect_tx(&C->full[s], stage_bytes);
+          mbar_arrive_expect_tx(&C->full[s], a_box_bytes + (uint32_t)BN * kBK * 2);
           const uint32_t a_dst = ring + (uint32_t)s * stage_bytes;
           tma_load_2d(a_dst, &P.tmA, kb * kBK, tm * kBM, &C->full[s]);
           tma_load_2d(a_dst + kBM * kBK * 2, &P.tmW, kb * kBK, tn * BN, &C->full[s]);
@@ -762,7 +766,8 @@ int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* 
   EncodeTiledFn fn = encode_fn(msg, cap);
   if (!fn) return -6;
   static thread_local CubeParams P;
-  if (!make_map(fn, &P.tmA, ptrs[ta.binding], K, M, pa, kBM) ||
+  const uint32_t a_rows = M >= (uint64_t)kBM ? (uint32_t)kBM : (uint32_t)((M + 7) / 8 * 8);
+  if (!make_map(fn, &P.tmA, ptrs[ta.binding], K, M, pa, a_rows) ||
       !make_map(fn, &P.tmW, ptrs[tw.binding], K, N, pw, (uint32_t)BN)) {
     std::snprintf(msg, cap, "cuTensorMapEncodeTiled rejected a MatMul operand");
     return -6;
