@@ -1,5 +1,6 @@
 """The C-ABI library on the host (no GPU): exports, bit-exact encoding against the
 reference encoder, golden images, fusion counts and validator rejections."""
+import ctypes
 import os
 import random
 import re
@@ -284,3 +285,35 @@ def test_graph_add_n_matches_op_by_op(name):
     finally:
         D.dvm_destroy(ctx)
     assert got == [img for img, _ in ref]
+
+
+def test_graph_add_n_rejects_bad_counts_and_keeps_earlier_ops():
+    ctx = D.dvm_create_host()
+    try:
+        a = D.dvm_input(ctx, "f32", [4, 256], None)
+        descs = (D.OpDesc * 3)()
+        for d, (op, n_in) in zip(descs, [("abs", 1), ("neg", 1), ("abs", 9)]):
+            d.op = D.OPS[op]
+            d.n_inputs = n_in
+            d.inputs[0] = a
+            d.rank = -1
+            d.out_dtype = D.DTYPES["f32"]
+        out = (ctypes.c_int32 * 3)(-7, -7, -7)
+        rc = D.lib().dvm_graph_add_n(ctx, descs, 3, out)
+        assert rc == -1                                   # INVALID_ARG from the third op
+        assert list(out) == [1, 2, -7]                     # the first two were appended
+        assert D.dvm_value_info(ctx, 2) == (D.DTYPES["f32"], (4, 256))
+        assert D.lib().dvm_graph_add_n(ctx, descs, -1, out) == -1
+        assert D.lib().dvm_graph_add_n(ctx, None, 0, None) == 0
+    finally:
+        D.dvm_destroy(ctx)
+
+
+def test_op_batch_splits_at_opaque_ops():
+    ops = [("abs", ["x"], "a", "f32", ()), ("opaque", [], "", "f32", ()),
+           ("neg", ["a"], "b", "f32", ()), ("muls", ["b"], "c", "f32", (2.0, 0))]
+    b = D.OpBatch(ops, ["x"], {"c"})
+    assert [len(d) for d, _, _, _ in b.packed] == [2, 2]
+    assert [opq for _, _, _, opq in b.packed] == [True, False]
+    assert b.ids == {"x": 0, "a": 1, "b": 2, "c": 3}
+    assert [list(e) for _, e, _, _ in b.packed] == [[1, -1], [2, 3]]
