@@ -120,8 +120,11 @@ class ClockSampler:
 class Workload:
     """Instance list + device pools + per-instance op feeding for one config."""
 
-    def __init__(self, name, rank, dev):
+    def __init__(self, name, rank, dev, pool_scale=1.0):
         import torch
+        # pool sizes (bytes for device_pool, elements for torch.empty), scaled down only
+        # for profiler captures of single instances
+        sc = lambda n: max(1 << 20, int(n * pool_scale))
         from bytecode_vm_jit_gb300 import workloads as W
         self.name, self.dev, self.W = name, dev, W
         self.torch = torch
@@ -131,46 +134,46 @@ class Workload:
             g, b, _ = W.layernorm_params()
             self.gamma = torch.from_numpy(g).to(dev)
             self.beta = torch.from_numpy(b).to(dev)
-            self.pool_x = W.device_pool(4 << 30, "f32", "normal", 101 + seed_off, dev)
-            self.pool_y = torch.empty(4 << 28, dtype=torch.float32, device=dev)
+            self.pool_x = W.device_pool(sc(4 << 30), "f32", "normal", 101 + seed_off, dev)
+            self.pool_y = torch.empty(sc(4 << 28), dtype=torch.float32, device=dev)
             self.d = W.LN_D
         elif name == "sqrt_add":
             self.sizes = [4096] * 16
-            self.pool_x = W.device_pool(1 << 30, "f32", "uniform", 100 + seed_off, dev)
-            self.pool_z = W.device_pool(1 << 30, "f32", "uniform", 200 + seed_off, dev)
-            self.pool_y = torch.empty(1 << 28, dtype=torch.float32, device=dev)
+            self.pool_x = W.device_pool(sc(1 << 30), "f32", "uniform", 100 + seed_off, dev)
+            self.pool_z = W.device_pool(sc(1 << 30), "f32", "uniform", 200 + seed_off, dev)
+            self.pool_y = torch.empty(sc(1 << 28), dtype=torch.float32, device=dev)
             self.d = 1024
         elif name == "if_else_add":
             self.sizes = W.if_else_rows()
-            self.pool_x = W.device_pool(4 << 30, "bf16", "normal", 102 + seed_off, dev)
-            self.pool_z = W.device_pool(4 << 30, "bf16", "normal", 202 + seed_off, dev)
-            self.pool_y = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+            self.pool_x = W.device_pool(sc(4 << 30), "bf16", "normal", 102 + seed_off, dev)
+            self.pool_z = W.device_pool(sc(4 << 30), "bf16", "normal", 202 + seed_off, dev)
+            self.pool_y = torch.empty(sc(2 << 30), dtype=torch.bfloat16, device=dev)
             self.d = W.IEA_D
         elif name == "qwen_stream":
             self.sizes = W.qwen_tokens()[:200]
             w, _ = W.qwen_weight()
             self.w = W.bf16_bits_to_torch(w).to(dev)
-            self.pool_x = W.device_pool(2 << 30, "bf16", "normal", 104 + seed_off, dev)
-            self.pool_z = W.device_pool(2 << 30, "bf16", "normal", 204 + seed_off, dev)
-            self.pool_g = W.device_pool(4 << 30, "bf16", "normal", 304 + seed_off, dev)
-            self.pool_u = W.device_pool(4 << 30, "bf16", "normal", 404 + seed_off, dev)
-            self.pool_y = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
-            self.pool_n = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
-            self.pool_s = torch.empty(2 << 30, dtype=torch.bfloat16, device=dev)
+            self.pool_x = W.device_pool(sc(2 << 30), "bf16", "normal", 104 + seed_off, dev)
+            self.pool_z = W.device_pool(sc(2 << 30), "bf16", "normal", 204 + seed_off, dev)
+            self.pool_g = W.device_pool(sc(4 << 30), "bf16", "normal", 304 + seed_off, dev)
+            self.pool_u = W.device_pool(sc(4 << 30), "bf16", "normal", 404 + seed_off, dev)
+            self.pool_y = torch.empty(sc(2 << 30), dtype=torch.bfloat16, device=dev)
+            self.pool_n = torch.empty(sc(1 << 30), dtype=torch.bfloat16, device=dev)
+            self.pool_s = torch.empty(sc(2 << 30), dtype=torch.bfloat16, device=dev)
         elif name == "addmm":
             self.sizes = W.matmul_rows()
             wt, _, _ = W.matmul_params()
             self.wt = W.bf16_bits_to_torch(wt).to(dev)
-            self.pool_x = W.device_pool(4 << 30, "bf16", "normal", 103 + seed_off, dev, std=0.02)
-            self.pool_c = W.device_pool(1 << 30, "bf16", "normal", 303 + seed_off, dev, std=0.1)
-            self.pool_y = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+            self.pool_x = W.device_pool(sc(4 << 30), "bf16", "normal", 103 + seed_off, dev, std=0.02)
+            self.pool_c = W.device_pool(sc(1 << 30), "bf16", "normal", 303 + seed_off, dev, std=0.1)
+            self.pool_y = torch.empty(sc(1 << 30), dtype=torch.bfloat16, device=dev)
         elif name == "matmul":
             self.sizes = W.matmul_rows()
             wt, bias, _ = W.matmul_params()
             self.wt = W.bf16_bits_to_torch(wt).to(dev)            # Wt[N,K]; W = Wt.t()
             self.bias = W.bf16_bits_to_torch(bias).to(dev)
-            self.pool_x = W.device_pool(4 << 30, "bf16", "normal", 103 + seed_off, dev, std=0.02)
-            self.pool_y = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+            self.pool_x = W.device_pool(sc(4 << 30), "bf16", "normal", 103 + seed_off, dev, std=0.02)
+            self.pool_y = torch.empty(sc(1 << 30), dtype=torch.bfloat16, device=dev)
         else:
             raise SystemExit("unknown config %s" % name)
         self.cursor = {}
@@ -400,6 +403,23 @@ def roofline_traffic(kernel_key):
     return ent.get("dram_bytes_per_unit"), ent
 
 
+def host_cpu():
+    """Model and logical core count of the host CPU (the encoder's and the oracle's)."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                k, _, v = ln.partition(":")
+                if k.strip() in ("model name", "Model", "CPU part") and v.strip():
+                    model = v.strip()
+                    if k.strip() == "model name":
+                        break
+    except OSError:
+        pass
+    return {"machine": platform.machine(), "model": model, "logical_cores": os.cpu_count()}
+
+
 # ------------------------------------------------------------------ main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -407,6 +427,9 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="dvm", choices=["dvm", "reference"])
+    ap.add_argument("--pool-scale", type=float, default=1.0,
+                    help="scale of the device input/output pools (below 1 only for profiler captures "
+                         "of a few instances; the pools then no longer defeat L2)")
     ap.add_argument("--config", default="layernorm", choices=["layernorm", "sqrt_add", "if_else_add", "qwen_stream", "matmul", "addmm"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--instances", type=int, default=0, help="use only the first N instances (profiling)")
@@ -467,7 +490,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    wl = Workload(args.config, rank, dev)
+    wl = Workload(args.config, rank, dev, args.pool_scale)
     if args.instances:
         wl.sizes = wl.sizes[:args.instances]
     if args.fixed_size:
@@ -482,9 +505,12 @@ def main():
     # feeds, fuses, encodes and launches every instance anew
     insts = [wl.instance(i) for i in range(n_inst)]
 
-    def step(events=None):
-        for ops, ins, outs in insts:
+    def step(events=None, owner=None):
+        for k, (ops, ins, outs) in enumerate(insts):
+            n0 = len(events) if events is not None else 0
             run.feed(ops, ins, outs, sptr, events)
+            if owner is not None:
+                owner.extend([k] * (len(events) - n0))   # the instance of each launch
 
     for _ in range(args.warmup):
         step()
@@ -520,10 +546,13 @@ def main():
     wall_us = [x / 1e3 for x in run.wall_ns]
 
     # ---------------- per-launch kernel durations for the roofline (separate pass)
-    events = []
-    step(events)
+    events, owner = [], []
+    step(events, owner)
     torch.cuda.synchronize()
     kernel_ms = sum(a.elapsed_time(b) for a, b in events)
+    inst_ms = [0.0] * n_inst
+    for (a, b), k in zip(events, owner):
+        inst_ms[k] += a.elapsed_time(b)
     kernel_gbs = wl.unit_bytes() / (kernel_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
     key = {"layernorm": "vm_vec_kernel<4>", "sqrt_add": "vm_vec_kernel<4>", "if_else_add": "vm_vec_kernel<8>",
@@ -555,6 +584,32 @@ def main():
                     "avg_launch_us": 1e3 * kernel_ms / max(1, len(events)),
                     "frac_of_nominal_8tbs": kernel_gbs / NOMINAL_HBM_GBS}
 
+    # per-size buckets of the dynamic instances (interpreter time only) and the latency
+    # of the small ones
+    if is_mm:
+        edges, label = [(1, 128), (128, 1024), (1024, 1 << 30)], "M"
+        size_of = lambda k: wl.sizes[k]
+        work_of = lambda k: wl.flops_of(wl.sizes[k]) / 1e12
+    else:
+        edges, label = [(0, 8 << 20), (8 << 20, 64 << 20), (64 << 20, 512 << 20), (512 << 20, 1 << 62)], "bytes"
+        size_of = lambda k: wl.bytes_of(wl.sizes[k])
+        work_of = lambda k: wl.bytes_of(wl.sizes[k]) / 1e9
+    denom = (load_tensor_peaks()[0] if is_mm else peak)
+    buckets = []
+    for lo_, hi_ in edges:
+        ks_ = [k for k in range(n_inst) if lo_ <= size_of(k) < hi_]
+        if not ks_:
+            continue
+        t = sum(inst_ms[k] for k in ks_) / 1e3
+        ach = sum(work_of(k) for k in ks_) / t if t > 0 else None
+        buckets.append({label: [lo_, hi_], "instances": len(ks_), "achieved": ach,
+                        "frac": ach / denom if ach else None,
+                        "median_instance_us": 1e3 * statistics.median(inst_ms[k] for k in ks_)})
+    roofline["buckets"] = buckets
+    small = sorted(range(n_inst), key=size_of)[:max(1, n_inst // 10)]
+    roofline["small_instance_latency_us"] = {"instances": len(small),
+                                             "median": 1e3 * statistics.median(inst_ms[k] for k in small)}
+
     # ---------------- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e and args.config == "layernorm":
@@ -580,6 +635,7 @@ def main():
             "encode_us_per_instance": {"median": statistics.median(enc_us), "p99": percentile(enc_us, 99),
                                        "source": "in-library host time (graph_add+flush+encode)"},
             "host_us_per_instance_python": {"median": statistics.median(wall_us), "p99": percentile(wall_us, 99)},
+            "host_cpu": host_cpu(),
             "clocks": clk, "gpu_launches": gpu_launches, "device_status": st,
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
         }
