@@ -31,6 +31,7 @@ constexpr int kVmReg = 64;          // fp32 values in ACC (and per slot) per thr
 constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 16384 padded elements per tile
 constexpr int kSmemBudget = 187392;  // DMA ring + hoist area of the VEC interpreter
 constexpr int kCubeRingBytes = 196608;  // TMA ring (A and W k-blocks) of the CUBE kernel
+constexpr int kCubeMaxStages = 32;      // stages of that ring (small-M instances have small stages)
 constexpr int kMaxRank = 4;
 
 enum KernelType : uint8_t { KT_VEC = 1, KT_CUBE = 2 };

@@ -879,7 +879,8 @@ void plan_cube(const dvm_ctx* c, Program& p) {
   p.t[1] = best_tn;
   p.t[2] = p.t[3] = 1;
   p.block_dim = best_tiles;
-  p.stage_bytes = (128 + best_tn) * 64 * 2;
+  // a stage holds the A box (min(128, M rounded up to 8) rows) and the W block, 64 K each
+  p.stage_bytes = (std::min<int64_t>(128, round_up(M, 8)) + best_tn) * 64 * 2;
   p.hoist_bytes = 0;
   p.K = K;
 }
@@ -1077,7 +1078,7 @@ size_t encode_launch(dvm_ctx* c, const std::vector<int32_t>& launch, std::vector
     block_dim += p->block_dim;
   }
   int64_t n_stages;
-  if (kernel_type == KT_CUBE) n_stages = std::min<int64_t>(D.max_stages, kCubeRingBytes / stage);
+  if (kernel_type == KT_CUBE) n_stages = std::min<int64_t>(kCubeMaxStages, kCubeRingBytes / stage);
   else n_stages = stage ? std::min<int64_t>(D.max_stages, (D.smem_budget - hoist_total) / stage) : 0;
   size_t off = sizeof(Header) + sizeof(ProgRec) * progs.size();
   std::vector<size_t> tens_off, body_off;
@@ -1507,9 +1508,11 @@ dvm_status dvm_validate(const uint8_t* img, size_t len) {
       if (pr.t[pr.rank - 1] % (32u * h.ve) || rows * pr.t[pr.rank - 1] > (uint64_t)kCapElems) return DVM_E_BYTECODE;
     } else {
       if (pr.rank != 2 || pr.t[0] != 128 || pr.t[1] % 16 || pr.t[1] > 256 || pr.K < 1) return DVM_E_BYTECODE;
-      // one MatMul program per launch; its TMA ring: stages of A [128 x 64] + W [t_N x 64] bf16
-      if (h.n_progs != 1 || h.n_stages < 2 || h.n_stages > 8) return DVM_E_BYTECODE;
-      if (h.stage_bytes != (128 + pr.t[1]) * 128 || (uint64_t)h.n_stages * h.stage_bytes > (uint64_t)kCubeRingBytes)
+      // one MatMul program per launch; its TMA ring: stages of the A box [min(128, M rounded
+      // up to 8) x 64] + W [t_N x 64] bf16
+      if (h.n_progs != 1 || h.n_stages < 2 || h.n_stages > kCubeMaxStages) return DVM_E_BYTECODE;
+      const uint64_t a_rows = pr.n[0] >= 128 ? 128 : (pr.n[0] + 7) / 8 * 8;
+      if (h.stage_bytes != (a_rows + pr.t[1]) * 128 || (uint64_t)h.n_stages * h.stage_bytes > (uint64_t)kCubeRingBytes)
         return DVM_E_BYTECODE;
     }
     TensRec tr[kMaxTens];

@@ -57,8 +57,8 @@ struct CubeParams {
 
 // shared-memory layout after the 1024-byte aligned ring
 struct CubeCtl {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t full[kCubeMaxStages];
+  uint64_t empty[kCubeMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -66,7 +66,8 @@ struct CubeCtl {
   int abort;
   int n_ep;   // decoded epilogue micro-ops
 };
-static_assert(sizeof(CubeCtl) <= 256, "control block");
+constexpr int kCubeCtlBytes = 1024;
+static_assert(sizeof(CubeCtl) <= kCubeCtlBytes, "control block");
 
 // ------------------------------------------------------------ TMA, tcgen05 --
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -556,8 +557,8 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
   const int S = H->n_stages;
   const uint32_t stage_bytes = H->stage_bytes;
   CubeCtl* C = reinterpret_cast<CubeCtl*>(smem + (size_t)S * stage_bytes);
-  EpOp* eops = reinterpret_cast<EpOp*>(smem + (size_t)S * stage_bytes + 256);
-  uint8_t* img = smem + (size_t)S * stage_bytes + 256 + kMaxEpOps * sizeof(EpOp);
+  EpOp* eops = reinterpret_cast<EpOp*>(smem + (size_t)S * stage_bytes + kCubeCtlBytes);
+  uint8_t* img = smem + (size_t)S * stage_bytes + kCubeCtlBytes + kMaxEpOps * sizeof(EpOp);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -582,9 +583,12 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
   const int M = (int)pr->n[0], N = (int)pr->n[1], K = (int)pr->K;
   const int BN = (int)pr->t[1];
   const int tiles_n = (N + BN - 1) / BN;
-  // A's TMA box is min(128, M rounded up to 8) rows: an instance with fewer than 128 rows
-  // copies only those (the rows of the A tile beyond them feed accumulator rows that the
-  // epilogue never stores)
+  // A's TMA box is min(128, M rounded up to 8) rows, and a stage holds only those rows
+  // followed by the W block: an instance with fewer than 128 rows copies no zero fill and
+  // fits more stages in the ring.  The MMA still reads a 128-row A operand; its rows
+  // beyond the box read whatever follows in shared memory (W, later stages, the control
+  // block, or the slack the launch allocates past them) and feed only accumulator rows
+  // that the epilogue never stores.
   const uint32_t a_box_bytes = (uint32_t)min(kBM, (M + 7) & ~7) * kBK * 2;
   const int nkb = (K + kBK - 1) / kBK;
   // two accumulators of BN columns, each starting on a multiple of 32 columns so that
@@ -609,17 +613,23 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
     if (lane == 0) {
       tma_prefetch_map(&P.tmA);
       tma_prefetch_map(&P.tmW);
-      int it = 0;
-      for (int tau = lo; tau < hi && !*abort; tau += step) {
+      // stage index, phase and destination advance incrementally: this thread issues a
+      // stage every few hundred cycles at the peak MMA rate, so the loop carries no
+      // division and no reload of anything but the barrier word
+      const uint32_t tx_bytes = a_box_bytes + (uint32_t)BN * kBK * 2;
+      int it = 0, s = 0;
+      uint32_t ph = 0, a_dst = ring;
+      bool ok = true;
+      for (int tau = lo; tau < hi && ok && !*abort; tau += step) {
         const int tm = tau / tiles_n, tn = tau - tm * tiles_n;
-        for (int kb = 0; kb < nkb; kb++, it++) {
-          const int s = it % S;
-          const uint32_t ph = (uint32_t)(it / S) & 1u;
-          if (!mbar_spin(&C->empty[s], ph ^ 1u, st, abort)) break;
-          mbar_arrive_expect_tx(&C->full[s], a_box_bytes + (uint32_t)BN * kBK * 2);
-          const uint32_t a_dst = ring + (uint32_t)s * stage_bytes;
-          tma_load_2d(a_dst, &P.tmA, kb * kBK, tm * kBM, &C->full[s]);
-          tma_load_2d(a_dst + kBM * kBK * 2, &P.tmW, kb * kBK, tn * BN, &C->full[s]);
+        const int ya = tm * kBM, yw = tn * BN;
+        for (int kx = 0; kx < nkb * kBK; kx += kBK, it++) {
+          if (!mbar_spin(&C->empty[s], ph ^ 1u, st, abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&C->full[s], tx_bytes);
+          tma_load_2d(a_dst, &P.tmA, kx, ya, &C->full[s]);
+          tma_load_2d(a_dst + a_box_bytes, &P.tmW, kx, yw, &C->full[s]);
+          a_dst += stage_bytes;
+          if (++s == S) { s = 0; ph ^= 1u; a_dst = ring; }
         }
       }
       // copies still in flight land before the CTA may exit (normally all have landed)
@@ -630,27 +640,34 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
     // ------------------------------------------------------------ MMA issuer --
     if (lane == 0) {
       const uint32_t idesc = mma_idesc(kBM, BN);
-      int it = 0, jt = 0;
-      bool issued = false;
-      for (int tau = lo; tau < hi && !*abort; tau += step, jt++) {
+      // the descriptors of stage 0; a stage further on adds stage_bytes >> 4 to the start
+      // address field (shared addresses stay below 2^18, so the field cannot carry)
+      const uint64_t da0 = sw128_desc(ring), db0 = sw128_desc(ring + a_box_bytes);
+      const uint64_t dstep = stage_bytes >> 4;
+      int jt = 0, s = 0;
+      uint32_t ph = 0;
+      uint64_t da = da0, db = db0;
+      bool issued = false, ok = true;
+      for (int tau = lo; tau < hi && ok && !*abort; tau += step, jt++) {
         const int b = jt & 1;
         const uint32_t use = (uint32_t)(jt >> 1);
         if (!mbar_spin(&C->tempty[b], (use & 1u) ^ 1u, st, abort)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * BNp);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; kb++, it++) {
-          const int s = it % S;
-          const uint32_t ph = (uint32_t)(it / S) & 1u;
+        uint32_t acc = 0;
+        for (int kb = 0; kb < nkb; kb++) {
           if (!mbar_spin(&C->full[s], ph, st, abort)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = ring + (uint32_t)s * stage_bytes;
-          const uint64_t da = sw128_desc(a_addr), db = sw128_desc(a_addr + kBM * kBK * 2);
 #pragma unroll
-          for (int k = 0; k < kBK / kUK; k++)
-            tc_mma(d, da + (uint64_t)(k * 2), db + (uint64_t)(k * 2), idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < kBK / kUK; k++) {
+            tc_mma(d, da + (uint64_t)(k * 2), db + (uint64_t)(k * 2), idesc, acc);
+            acc = 1u;
+          }
           issued = true;
           tc_commit(&C->empty[s]);
+          da += dstep;
+          db += dstep;
+          if (++s == S) { s = 0; ph ^= 1u; da = da0; db = db0; }
         }
         if (!ok) break;
         tc_commit(&C->tfull[b]);
@@ -751,8 +768,10 @@ int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* 
   std::memcpy(&tw, image + pr.tens_off + w1.b * sizeof(TensRec), sizeof tw);
   const uint64_t M = pr.n[0], N = pr.n[1], K = pr.K, BN = pr.t[1];
   const size_t ring = (size_t)h.n_stages * h.stage_bytes;
+  const uint32_t a_rows = M >= (uint64_t)kBM ? (uint32_t)kBM : (uint32_t)((M + 7) / 8 * 8);
   if (ta.dtype != DT_BF16 || tw.dtype != DT_BF16 || ta.vs[1] != 1 || tw.vs[0] != 1 || h.n_stages < 2 ||
-      h.n_stages > 8 || h.stage_bytes != (uint32_t)((kBM + BN) * kBK * 2) || ring > (size_t)kCubeRingBytes) {
+      h.n_stages > kCubeMaxStages || h.stage_bytes != (uint32_t)((a_rows + BN) * kBK * 2) ||
+      ring > (size_t)kCubeRingBytes) {
     std::snprintf(msg, cap, "CUBE operands must be bf16 and K-contiguous with a valid stage ring");
     return -5;
   }
@@ -766,7 +785,6 @@ int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* 
   EncodeTiledFn fn = encode_fn(msg, cap);
   if (!fn) return -6;
   static thread_local CubeParams P;
-  const uint32_t a_rows = M >= (uint64_t)kBM ? (uint32_t)kBM : (uint32_t)((M + 7) / 8 * 8);
   if (!make_map(fn, &P.tmA, ptrs[ta.binding], K, M, pa, a_rows) ||
       !make_map(fn, &P.tmW, ptrs[tw.binding], K, N, pw, (uint32_t)BN)) {
     std::snprintf(msg, cap, "cuTensorMapEncodeTiled rejected a MatMul operand");
@@ -777,7 +795,12 @@ int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* 
   for (int i = 0; i < n; i++) P.ptrs[i] = ptrs[i];
   P.status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(st->scratch) + 8);
   P.timeout_ns = (unsigned long long)st->timeout_ms * 1000000ull;
-  const size_t smem = 1024 + ring + 256 + kMaxEpOps * sizeof(EpOp) + P.image_len;
+  // the last stage's 128-row A operand may reach (128 - a_rows) rows of 128 bytes past its
+  // own A box and W block: the allocation covers that reach whatever follows the ring
+  const size_t tail = (size_t)kCubeCtlBytes + kMaxEpOps * sizeof(EpOp) + P.image_len;
+  const size_t reach = (size_t)(kBM - a_rows) * kBK * 2;
+  const size_t over = reach > BN * kBK * 2 ? reach - BN * kBK * 2 : 0;
+  const size_t smem = 1024 + ring + (over > tail ? over : tail);
   if ((int)smem > st->max_smem_optin) {
     std::snprintf(msg, cap, "CUBE shared memory %zu exceeds the device limit %d", smem, st->max_smem_optin);
     return -8;

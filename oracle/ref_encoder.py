@@ -52,6 +52,7 @@ KT_VEC, KT_CUBE = 1, 2
 MAGIC = 0x314D5644
 MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
 CUBE_RING_BYTES = 196608   # shared-memory ring of the MatMul tile op (A and W k-blocks)
+CUBE_MAX_STAGES = 32       # stages of that ring
 
 DEFAULT_DESC = dict(num_cores=152, cap_elems=16384, smem_budget=187392, max_stages=8,
                     c0_bytes=65536, flops_per_byte=280, n_slots=2)
@@ -866,7 +867,8 @@ class RefCtx:
             if ins["op"] == I_LD:
                 ten = prog["tensors"][ins["b"]]
                 ins["flags"] = L_ROWV if ten["vs"][1] == 0 else 0
-        stage = (128 + tn) * 64 * 2
+        # one stage: the A box (M rounded up to 8 rows, at most 128) and the W block, 64 K each
+        stage = (min(128, round_up(M, 8)) + tn) * 64 * 2
         prog.update(t=[128, tn], block_dim=tiles, stage_bytes=stage, hoist_bytes=0, K=K)
 
     # -- bytes
@@ -920,7 +922,7 @@ class RefCtx:
         stage = max(p["stage_bytes"] for p in progs)
         hoist_total = sum(p["hoist_bytes"] for p in progs)
         if kernel_type == KT_CUBE:
-            n_stages = min(d_["max_stages"], CUBE_RING_BYTES // stage)
+            n_stages = min(CUBE_MAX_STAGES, CUBE_RING_BYTES // stage)
         else:
             n_stages = min(d_["max_stages"], (d_["smem_budget"] - hoist_total) // stage) if stage else 0
         # offsets

@@ -256,3 +256,21 @@ def test_interp_mixed_ops_and_row_values():
     ref = evaluate(ops, inp)
     _cmp(got["o3"], ref["o3"], 1e-5)
     _cmp(got["s"], ref["s"], 1e-5)
+
+
+@pytest.mark.parametrize("m", [1, 7, 8, 9, 64, 127, 128, 300, 8192])
+def test_cube_ring_stages(m):
+    """The MatMul ring: a stage is the A box (m rounded up to 8 rows, at most 128) plus
+    the W block of t_N rows, 128 bytes (64 bf16) each, 1 KiB-aligned for the 128-byte
+    swizzle; as many stages as the 192 KiB ring holds, at most 32."""
+    l, p = _counts(W.MATMUL_ABS_OPS, {"A": ("bf16", (m, 4096)), "W": ("bf16", (4096, 4096)),
+                                      "bias": ("bf16", (4096,))}, W.MATMUL_ABS_OUT,
+                   strides={"W": [1, 4096]})
+    h = parse(l[0][0])[0]
+    tn = p[0][0]["t"][1]
+    a_rows = 128 if m >= 128 else -(-m // 8) * 8
+    assert h["stage_bytes"] == (a_rows + tn) * 128 and h["stage_bytes"] % 1024 == 0
+    assert h["n_stages"] == min(32, 196608 // h["stage_bytes"])
+    assert 2 <= h["n_stages"] and h["n_stages"] * h["stage_bytes"] <= 196608
+    if m <= 8:
+        assert h["n_stages"] == 32   # small instances keep 32 k-blocks in flight
