@@ -32,6 +32,13 @@ constexpr int kCapElems = kVmWarps * 32 * kVmReg;  // 16384 padded elements per 
 constexpr int kSmemBudget = 187392;  // DMA ring + hoist area of the VEC interpreter
 constexpr int kCubeRingBytes = 196608;  // TMA ring (A and W k-blocks) of the CUBE kernel
 constexpr int kCubeMaxStages = 32;      // stages of that ring (small-M instances have small stages)
+// Split-K MatMul tiles: fp32 partial tiles of [128 x t_N] per K-split, and one arrival
+// counter per output tile, in a workspace of the context
+constexpr int64_t kCubeWsBytes = 32ll << 20;
+constexpr int kCubeWsTiles = 4096;
+// the MMA thread's fixed work per 64-deep k-block (four MMA issues, a barrier wait and a
+// commit: ~400 cycles), in bytes at one SM's share of HBM bandwidth, for the tiler's cost
+constexpr int64_t kCubeKbCost = 8192;
 constexpr int kMaxRank = 4;
 
 enum KernelType : uint8_t { KT_VEC = 1, KT_CUBE = 2 };

@@ -855,20 +855,33 @@ void plan_cube(const dvm_ctx* c, Program& p) {
   int out_esz = 4;
   for (const Ins& w : body)
     if (w.op == OP_ST) out_esz = std::min(out_esz, dtype_size(p.tensors[w.a].dtype));
-  int64_t best_cost = -1, best_tn = 0, best_tiles = 0;
+  // candidates: t_N halved from N (16-aligned, <= 256) x K split into ks tiles of t_K
+  // (64-aligned); a split tile writes and the last one re-reads fp32 partials
+  int64_t best_cost = -1, best_tn = 0, best_tk = 0, best_tiles = 0;
   for (int64_t k = 1;; k *= 2) {
     int64_t cc = cdiv(N, k);
     int64_t tn = round_up(cc, 16);
     if (tn <= 256) {
-      int64_t tiles = cdiv(M, 128) * cdiv(N, tn);
-      int64_t waves = cdiv(tiles, D.num_cores);
-      int64_t flops = 2 * 128 * tn * K;
-      int64_t tb = (128 + tn) * K * 2 + 128 * tn * out_esz;
-      int64_t cost = waves * std::max(cdiv(flops, D.flops_per_byte), tb);
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best_tn = tn;
-        best_tiles = tiles;
+      int64_t tiles_mn = cdiv(M, 128) * cdiv(N, tn);
+      for (int64_t ks = 1; ks <= 32; ks *= 2) {
+        int64_t tk = round_up(cdiv(K, ks), 64);
+        if (cdiv(K, tk) != ks && ks > 1) continue;
+        // K-splits only for instances of one row tile (M <= 128), within the workspace
+        if (ks > 1 && (M > 128 || tiles_mn > kCubeWsTiles || ks * tiles_mn * 128 * tn * 4 > kCubeWsBytes)) continue;
+        int64_t tiles = tiles_mn * ks;
+        int64_t waves = cdiv(tiles, D.num_cores);
+        int64_t flops = 2 * 128 * tn * tk;
+        int64_t tb = (128 + tn) * tk * 2 + (ks > 1 ? 2 * 128 * tn * 4 : 128 * tn * out_esz);
+        // the CTA completing a split tile reads every split's partial rows: a serial,
+        // latency-bound tail (weighted 4x a streamed byte)
+        int64_t tail = ks > 1 ? 4 * ks * M * tn * 4 : 0;
+        int64_t cost = waves * (std::max(cdiv(flops, D.flops_per_byte), tb) + cdiv(tk, 64) * kCubeKbCost) + tail;
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best_tn = tn;
+          best_tk = tk;
+          best_tiles = tiles;
+        }
       }
     }
     if (tn <= 16) break;
@@ -877,7 +890,8 @@ void plan_cube(const dvm_ctx* c, Program& p) {
     if (w.op == OP_LD) w.flags = p.tensors[w.b].vs[1] == 0 ? LF_ROWV : 0;
   p.t[0] = 128;
   p.t[1] = best_tn;
-  p.t[2] = p.t[3] = 1;
+  p.t[2] = best_tk;
+  p.t[3] = 1;
   p.block_dim = best_tiles;
   // a stage holds the A box (min(128, M rounded up to 8) rows) and the W block, 64 K each
   p.stage_bytes = (std::min<int64_t>(128, round_up(M, 8)) + best_tn) * 64 * 2;
@@ -1124,7 +1138,7 @@ size_t encode_launch(dvm_ctx* c, const std::vector<int32_t>& launch, std::vector
     pr.tens_off = (uint32_t)tens_off[i];
     for (int d = 0; d < 4; d++) {
       pr.n[d] = d < p->G.rank ? (uint32_t)p->G.d[d] : 1;
-      pr.t[d] = d < p->G.rank ? (uint32_t)p->t[d] : 1;
+      pr.t[d] = d < p->G.rank || (p->kind == PK_CUBE && d == 2) ? (uint32_t)p->t[d] : 1;  // MatMul: t_K third
     }
     pr.K = (uint32_t)p->K;
     pr.hoist_base = hbase;
@@ -1497,6 +1511,12 @@ dvm_status dvm_validate(const uint8_t* img, size_t len) {
     uint64_t tiles = 1;
     for (int d = 0; d < 4; d++) {
       if (pr.n[d] < 1 || pr.t[d] < 1) return DVM_E_BYTECODE;
+      // a MatMul tile's third extent is its K-extent t_K (the K-split)
+      if (pr.kind == PK_CUBE && d == 2) {
+        if (pr.n[d] != 1 || pr.K < 1 || pr.t[d] % 64) return DVM_E_BYTECODE;
+        tiles *= (pr.K + pr.t[d] - 1) / pr.t[d];
+        continue;
+      }
       if (d >= pr.rank && (pr.n[d] != 1 || pr.t[d] != 1)) return DVM_E_BYTECODE;
       tiles *= (pr.n[d] + pr.t[d] - 1) / pr.t[d];
     }
@@ -1508,6 +1528,11 @@ dvm_status dvm_validate(const uint8_t* img, size_t len) {
       if (pr.t[pr.rank - 1] % (32u * h.ve) || rows * pr.t[pr.rank - 1] > (uint64_t)kCapElems) return DVM_E_BYTECODE;
     } else {
       if (pr.rank != 2 || pr.t[0] != 128 || pr.t[1] % 16 || pr.t[1] > 256 || pr.K < 1) return DVM_E_BYTECODE;
+      // a K-split needs its partial tiles and counters to fit the context's workspace
+      const uint64_t ks = (pr.K + pr.t[2] - 1) / pr.t[2];
+      const uint64_t tiles_mn = pr.block_dim / ks;
+      if (ks > 1 && (tiles_mn > (uint64_t)kCubeWsTiles || ks * tiles_mn * 128 * pr.t[1] * 4 > (uint64_t)kCubeWsBytes))
+        return DVM_E_BYTECODE;
       // one MatMul program per launch; its TMA ring: stages of the A box [min(128, M rounded
       // up to 8) x 64] + W [t_N x 64] bf16
       if (h.n_progs != 1 || h.n_stages < 2 || h.n_stages > kCubeMaxStages) return DVM_E_BYTECODE;

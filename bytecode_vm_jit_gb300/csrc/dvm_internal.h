@@ -17,6 +17,9 @@ struct DeviceState {
   int skip_arrival = 0;           // test hook: next barrier skips one arrival
   int timeout_ms = 2000;          // bounded waits
   int launches = 0;
+  void* cube_ws = nullptr;        // K-split MatMul workspace (kCubeWsBytes of fp32 partial
+                                  // tiles, then kCubeWsTiles i32 arrival counters), allocated
+                                  // at the context's first K-split launch
 };
 
 constexpr size_t kScratchBytes = 64 + 4 * 1024;

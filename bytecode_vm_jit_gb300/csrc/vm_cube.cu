@@ -51,6 +51,8 @@ struct CubeParams {
   alignas(16) uint8_t image[kMaxImage];
   void* ptrs[kMaxBind];
   int32_t* status;
+  float* ws;               // K-split partial tiles: [output tile][split][128 rows][t_N] fp32
+  int* ws_count;           // K-split arrivals per output tile (zero between launches)
   unsigned long long timeout_ns;
   uint32_t image_len;
 };
@@ -62,9 +64,11 @@ struct CubeCtl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t esync;   // the epilogue warps' barrier (bounded waits)
   uint32_t tmem_base;
   int abort;
-  int n_ep;   // decoded epilogue micro-ops
+  int n_ep;         // decoded epilogue micro-ops
+  int ep_last[2];   // this CTA completes the output tile of its K-split (by tile parity)
 };
 constexpr int kCubeCtlBytes = 1024;
 static_assert(sizeof(CubeCtl) <= kCubeCtlBytes, "control block");
@@ -152,6 +156,15 @@ __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const 
       return false;
     }
   }
+}
+
+// barrier of the four epilogue warps on an mbarrier of 128 arrivals: a bounded wait, so a
+// warp that left its loop on abort cannot hold the others forever
+__device__ __forceinline__ bool ep_sync(uint64_t* bar, uint32_t& ph, const DevStatus& st, volatile int* abort) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, ph, st, abort);
+  ph ^= 1u;
+  return ok;
 }
 
 // bounded wait that ignores the abort flag (draining copies and MMAs before exit)
@@ -576,6 +589,7 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
       mbar_init(&C->tempty[b], 128);
     }
     mbar_init(&C->drain, 1);
+    mbar_init(&C->esync, 128);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -583,6 +597,9 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
   const int M = (int)pr->n[0], N = (int)pr->n[1], K = (int)pr->K;
   const int BN = (int)pr->t[1];
   const int tiles_n = (N + BN - 1) / BN;
+  // a work unit is one K-split of one output tile: unit = tile * ks + split
+  const int TK = (int)pr->t[2];
+  const int ks = (K + TK - 1) / TK;
   // A's TMA box is min(128, M rounded up to 8) rows, and a stage holds only those rows
   // followed by the W block: an instance with fewer than 128 rows copies no zero fill and
   // fits more stages in the ring.  The MMA still reads a 128-row A operand; its rows
@@ -590,7 +607,6 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
   // block, or the slack the launch allocates past them) and feed only accumulator rows
   // that the epilogue never stores.
   const uint32_t a_box_bytes = (uint32_t)min(kBM, (M + 7) & ~7) * kBK * 2;
-  const int nkb = (K + kBK - 1) / kBK;
   // two accumulators of BN columns, each starting on a multiple of 32 columns so that
   // the epilogue's 32-column reads stay inside the accumulator they belong to
   const int BNp = (BN + 31) & ~31;
@@ -621,9 +637,11 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
       uint32_t ph = 0, a_dst = ring;
       bool ok = true;
       for (int tau = lo; tau < hi && ok && !*abort; tau += step) {
-        const int tm = tau / tiles_n, tn = tau - tm * tiles_n;
+        const int tile = tau / ks, kk = tau - tile * ks;
+        const int tm = tile / tiles_n, tn = tile - tm * tiles_n;
         const int ya = tm * kBM, yw = tn * BN;
-        for (int kx = 0; kx < nkb * kBK; kx += kBK, it++) {
+        const int k1 = min(K, (kk + 1) * TK);
+        for (int kx = kk * TK; kx < k1; kx += kBK, it++) {
           if (!mbar_spin(&C->empty[s], ph ^ 1u, st, abort)) { ok = false; break; }
           mbar_arrive_expect_tx(&C->full[s], tx_bytes);
           tma_load_2d(a_dst, &P.tmA, kx, ya, &C->full[s]);
@@ -654,8 +672,10 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
         if (!mbar_spin(&C->tempty[b], (use & 1u) ^ 1u, st, abort)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * BNp);
+        const int kk = tau % ks;
+        const int nkb_u = (min(K, (kk + 1) * TK) - kk * TK + kBK - 1) / kBK;
         uint32_t acc = 0;
-        for (int kb = 0; kb < nkb; kb++) {
+        for (int kb = 0; kb < nkb_u; kb++) {
           if (!mbar_spin(&C->full[s], ph, st, abort)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -690,22 +710,107 @@ __global__ void __launch_bounds__(kCubeThreads, 1) vm_cube_kernel(const __grid_c
     named_bar(2, 128);
     const int ne = C->n_ep;
     int jt = 0;
+    uint32_t eph = 0;
     for (int tau = lo; tau < hi; tau += step, jt++) {
       const int b = jt & 1;
       if (!mbar_wait(&C->tfull[b], (uint32_t)(jt >> 1) & 1u, st, abort)) break;
       tc_fence_after();
-      const int tm = tau / tiles_n, tn = tau - tm * tiles_n;
+      const int tile = tau / ks;
+      const int tm = tile / tiles_n, tn = tile - tm * tiles_n;
       const int m = tm * kBM + row;
       const bool row_ok = m < M;
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BNp);
+      if (ks == 1) {
+        for (int c = 0; c < BN; c += 32) {
+          const int n0 = tn * BN + c;
+          if (n0 >= N) break;  // warp-uniform
+          float acc[32];
+          tc_ld32(tacc + (uint32_t)c, acc);
+          run_epilogue(eops, ne, acc, m, row_ok, n0, min(min(32, BN - c), N - n0));
+        }
+        tc_fence_before();
+        mbar_arrive(&C->tempty[b]);
+        continue;
+      }
+      // K-split: store this split's fp32 partial rows, count the split in; the CTA that
+      // brings the count to ks sums the partials in split order and runs the epilogue
+      float* own = P.ws + ((size_t)tau * kBM + row) * BN;
       for (int c = 0; c < BN; c += 32) {
-        const int n0 = tn * BN + c;
-        if (n0 >= N) break;  // warp-uniform
         float acc[32];
-        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BNp + c), acc);
-        run_epilogue(eops, ne, acc, m, row_ok, n0, min(min(32, BN - c), N - n0));
+        tc_ld32(tacc + (uint32_t)c, acc);
+        if (row_ok) {
+          float4* d4 = reinterpret_cast<float4*>(own + c);
+#pragma unroll
+          for (int i = 0; i < 8; i++)
+            if (c + 4 * i < BN) d4[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        }
       }
       tc_fence_before();
       mbar_arrive(&C->tempty[b]);
+      __threadfence();
+      if (!ep_sync(&C->esync, eph, st, abort)) break;
+      if (threadIdx.x == 64) {
+        const int old = atomicAdd(P.ws_count + tile, 1);
+        const int last = old == ks - 1 ? 1 : 0;
+        if (last) P.ws_count[tile] = 0;  // every split of this launch has counted in
+        C->ep_last[jt & 1] = last;
+        __threadfence();
+      }
+      if (!ep_sync(&C->esync, eph, st, abort)) break;
+      if (!*reinterpret_cast<volatile int*>(&C->ep_last[jt & 1])) continue;
+      __threadfence();
+      // this CTA completes the tile.  (1) the 128 epilogue threads sum the splits' float4
+      // columns in split order, in place over split 0; (2) they run the epilogue over
+      // (row, 32-column) chunks of the sum.  Both spread the tile over all threads, so a
+      // tile of few rows is summed as fast as a full one per byte.
+      const int et = threadIdx.x - 64;
+      const int rows_v = min(kBM, M - tm * kBM), cols_v = min(BN, N - tn * BN);
+      float* part = P.ws + (size_t)tile * ks * kBM * BN;
+      const size_t sstride = (size_t)kBM * BN / 4;  // float4s between splits
+      const int nf4 = (cols_v + 3) / 4, n_sum = rows_v * nf4;
+      constexpr int U = 4;
+      for (int i0 = et; i0 < n_sum; i0 += 128 * U) {
+        float4 a[U];
+        float4* p4[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+          const int i = min(i0 + u * 128, n_sum - 1);
+          const int r = i / nf4;
+          p4[u] = reinterpret_cast<float4*>(part + (size_t)r * BN) + (i - r * nf4);
+          a[u] = __ldcg(p4[u]);
+        }
+#pragma unroll 4
+        for (int sp = 1; sp < ks; sp++) {
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const float4 v = __ldcg(p4[u] + sp * sstride);
+            a[u].x += v.x;
+            a[u].y += v.y;
+            a[u].z += v.z;
+            a[u].w += v.w;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++)
+          if (i0 + u * 128 < n_sum) __stcg(p4[u], a[u]);
+      }
+      if (!ep_sync(&C->esync, eph, st, abort)) break;
+      const int nch = (cols_v + 31) / 32;
+      for (int i = et; i < rows_v * nch; i += 128) {
+        const int r = i / nch, c = (i - r * nch) * 32;
+        const float4* s4 = reinterpret_cast<const float4*>(part + (size_t)r * BN + c);
+        float acc[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; q4++) {
+          const float4 v = c + 4 * q4 < BN ? __ldcg(s4 + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          acc[4 * q4] = v.x;
+          acc[4 * q4 + 1] = v.y;
+          acc[4 * q4 + 2] = v.z;
+          acc[4 * q4 + 3] = v.w;
+        }
+        run_epilogue(eops, ne, acc, tm * kBM + r, true, tn * BN + c, min(32, cols_v - c));
+      }
+      if (!ep_sync(&C->esync, eph, st, abort)) break;
     }
   }
 
@@ -795,6 +900,22 @@ int cube_launch(DeviceState* st, const uint8_t* image, size_t len, void* const* 
   for (int i = 0; i < n; i++) P.ptrs[i] = ptrs[i];
   P.status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(st->scratch) + 8);
   P.timeout_ns = (unsigned long long)st->timeout_ms * 1000000ull;
+  // K-split tiles: the context's workspace, allocated at its first K-split launch
+  const uint64_t TK = pr.t[2];
+  if ((K + TK - 1) / TK > 1 && !st->cube_ws) {
+    const size_t bytes = (size_t)kCubeWsBytes + sizeof(int) * kCubeWsTiles;
+    void* ws = nullptr;
+    cudaError_t e = cudaMalloc(&ws, bytes);
+    if (e == cudaSuccess) e = cudaMemset(static_cast<uint8_t*>(ws) + kCubeWsBytes, 0, sizeof(int) * kCubeWsTiles);
+    if (e != cudaSuccess) {
+      if (ws) cudaFree(ws);
+      std::snprintf(msg, cap, "K-split workspace allocation failed: %s", cudaGetErrorString(e));
+      return -6;
+    }
+    st->cube_ws = ws;
+  }
+  P.ws = static_cast<float*>(st->cube_ws);
+  P.ws_count = st->cube_ws ? reinterpret_cast<int*>(static_cast<uint8_t*>(st->cube_ws) + kCubeWsBytes) : nullptr;
   // the last stage's 128-row A operand may reach (128 - a_rows) rows of 128 bytes past its
   // own A box and W block: the allocation covers that reach whatever follows the ring
   const size_t tail = (size_t)kCubeCtlBytes + kMaxEpOps * sizeof(EpOp) + P.image_len;

@@ -55,8 +55,10 @@ void device_free(DeviceState* st) {
     cudaGetDevice(&prev);
     cudaSetDevice(st->device);
     cudaFree(st->scratch);
+    if (st->cube_ws) cudaFree(st->cube_ws);
     cudaSetDevice(prev);
     st->scratch = nullptr;
+    st->cube_ws = nullptr;
   }
 }
 
@@ -114,8 +116,11 @@ int device_poll(DeviceState* st, void* stream, int32_t* status, char* msg, size_
   int32_t word = 0;
   if (e == cudaSuccess) e = cudaMemcpy(&word, static_cast<uint8_t*>(st->scratch) + 8, 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && word != 0) {
-    // clear the status word and re-initialise the grid barrier
+    // clear the status word and re-initialise the grid barrier and the K-split counters
+    // (an aborted launch can leave them part-counted)
     e = cudaMemset(st->scratch, 0, 64);
+    if (e == cudaSuccess && st->cube_ws)
+      e = cudaMemset(static_cast<uint8_t*>(st->cube_ws) + kCubeWsBytes, 0, sizeof(int) * kCubeWsTiles);
     st->barrier_base = 0;
   }
   if (prev != st->device) cudaSetDevice(prev);

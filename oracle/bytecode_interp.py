@@ -251,7 +251,10 @@ class Interp:
         return _f32(a @ wm)
 
     def run_cube(self, prog):
-        for tau in range(prog["block_dim"]):
+        # K-split tiles of one output block together compute the block's full product:
+        # each output block is evaluated once, over all of K
+        ks = -(-prog["K"] // prog["t"][2])
+        for tau in range(prog["block_dim"] // ks):
             self.exec_tile(prog, tau, prog["body"][1:1 + prog["body"][0]["imm"]], {})
 
 

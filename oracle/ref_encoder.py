@@ -53,6 +53,9 @@ MAGIC = 0x314D5644
 MAX_PROGS, MAX_BIND, MAX_TENS, MAX_INSTR, MAX_IMAGE = 4, 16, 16, 96, 8192
 CUBE_RING_BYTES = 196608   # shared-memory ring of the MatMul tile op (A and W k-blocks)
 CUBE_MAX_STAGES = 32       # stages of that ring
+CUBE_WS_BYTES = 32 << 20   # fp32 partial tiles of K-split MatMul tiles
+CUBE_WS_TILES = 4096       # arrival counters (output tiles) of K-split MatMul tiles
+CUBE_KB_COST = 8192        # fixed MMA-issue work per 64-deep k-block, in bytes, for the tiler
 
 DEFAULT_DESC = dict(num_cores=152, cap_elems=16384, smem_budget=187392, max_stages=8,
                     c0_bytes=65536, flops_per_byte=280, n_slots=2)
@@ -845,23 +848,38 @@ class RefCtx:
         for ins in mm_body:
             if ins["op"] == I_ST:
                 out_esz = min(out_esz, ESZ[prog["tensors"][ins["a"]]["dtype"]])
+        # tile candidates: t_N halved from N (16-aligned, at most 256), and K split into
+        # ks tiles of t_K (64-aligned); a split tile stores fp32 partials that the last
+        # tile of its output block reads back
         best = None
         k = 1
         while True:
             c = cdiv(N, k)
             tn = round_up(c, 16)
             if tn <= 256:
-                tiles = cdiv(M, 128) * cdiv(N, tn)
-                waves = cdiv(tiles, d_["num_cores"])
-                flops = 2 * 128 * tn * K
-                tb = (128 + tn) * K * 2 + 128 * tn * out_esz
-                cost = waves * max(cdiv(flops, d_["flops_per_byte"]), tb)
-                if best is None or cost < best[0]:
-                    best = (cost, tn, tiles)
+                tiles_mn = cdiv(M, 128) * cdiv(N, tn)
+                ks = 1
+                while ks <= 32:
+                    tk = round_up(cdiv(K, ks), 64)
+                    # K-splits only for instances of one row tile (M <= 128), within the workspace
+                    usable = ks == 1 or (cdiv(K, tk) == ks and M <= 128 and tiles_mn <= CUBE_WS_TILES
+                                         and ks * tiles_mn * 128 * tn * 4 <= CUBE_WS_BYTES)
+                    if usable:
+                        tiles = tiles_mn * ks
+                        waves = cdiv(tiles, d_["num_cores"])
+                        flops = 2 * 128 * tn * tk
+                        tb = (128 + tn) * tk * 2 + (2 * 128 * tn * 4 if ks > 1 else 128 * tn * out_esz)
+                        # the tile completing a split reads every split's partial rows: a
+                        # serial, latency-bound tail (weighted 4x a streamed byte)
+                        tail = 4 * ks * M * tn * 4 if ks > 1 else 0
+                        cost = waves * (max(cdiv(flops, d_["flops_per_byte"]), tb) + cdiv(tk, 64) * CUBE_KB_COST) + tail
+                        if best is None or cost < best[0]:
+                            best = (cost, tn, tk, tiles)
+                    ks *= 2
             if tn <= 16:
                 break
             k *= 2
-        _, tn, tiles = best
+        _, tn, tk, tiles = best
         # every epilogue load is direct in the cube VM
         for ins in mm_body:
             if ins["op"] == I_LD:
@@ -869,7 +887,7 @@ class RefCtx:
                 ins["flags"] = L_ROWV if ten["vs"][1] == 0 else 0
         # one stage: the A box (M rounded up to 8 rows, at most 128) and the W block, 64 K each
         stage = (min(128, round_up(M, 8)) + tn) * 64 * 2
-        prog.update(t=[128, tn], block_dim=tiles, stage_bytes=stage, hoist_bytes=0, K=K)
+        prog.update(t=[128, tn, tk], block_dim=tiles, stage_bytes=stage, hoist_bytes=0, K=K)
 
     # -- bytes
     def encode(self, li):
@@ -948,7 +966,7 @@ class RefCtx:
         hbase = 0
         for p, to, bo, s in zip(progs, tens_offs, body_offs, streams):
             n4 = list(p["G"]) + [1] * (4 - p["rank"])
-            t4 = list(p["t"]) + [1] * (4 - p["rank"])
+            t4 = (list(p["t"]) + [1] * 4)[:4]   # a MatMul tile carries t_K third
             out += struct.pack("<IIBBBBIII", p["block_dim"], base, p["rank"], len(p["tensors"]),
                                p["kind"], 0, bo, len(s), to)
             out += struct.pack("<4I", *n4) + struct.pack("<4I", *t4)

@@ -8,6 +8,8 @@ products are accumulated in fp32 over K = 4096 terms, so the fp32 element-wise
 bound of 1e-5 does not apply to the matmul itself).  Identity and zero weights
 give exact results.
 """
+import struct
+
 import numpy as np
 import pytest
 import torch
@@ -103,7 +105,8 @@ def test_matmul_abs_largest_instance_sampled_rows():
 
 # --------------------------------------------------- brute force, tiny shapes --
 @pytest.mark.parametrize("m,n,k", [(1, 1, 1), (7, 7, 7), (64, 64, 64), (128, 128, 128), (129, 129, 129),
-                                   (1, 129, 64), (129, 7, 128), (7, 300, 129), (200, 48, 1000)])
+                                   (1, 129, 64), (129, 7, 128), (7, 300, 129), (200, 48, 1000),
+                                   (5, 600, 3000), (130, 520, 2048)])
 def test_matmul_brute_force(m, n, k):
     rng = np.random.default_rng(m * 10007 + n * 101 + k)
     a = W.f32_to_bf16_bits(rng.standard_normal((m, k)).astype(np.float32))
@@ -118,6 +121,32 @@ def test_matmul_brute_force(m, n, k):
             ref[i, j] = abs(float(np.dot(af[i], wf[j])) + bf[j]) * 0.5
     from oracle.bf16 import round_bf16
     check_bf16(got, round_bf16(ref))
+
+
+def test_k_split_repeated_launches_agree():
+    """Few-row MatMuls run as K-split tiles whose per-tile arrival counters live in the
+    context's workspace and return to zero after every launch: the same instance run
+    three times in one context gives the same bits each time, and matches the oracle."""
+    wt, bias, _ = W.matmul_params()
+    wt_d, bias_d = dev_bf16(wt), dev_bf16(bias)
+    rng = np.random.default_rng(31)
+    a = W.f32_to_bf16_bits((rng.standard_normal((3, 4096)) * 0.02).astype(np.float32))
+    a_d = dev_bf16(a)
+    ctx = D.Ctx(0)
+    try:
+        outs = []
+        for _ in range(3):
+            ctx.reset()
+            out = ctx.feed(W.MATMUL_ABS_OPS, {"A": a_d, "W": wt_d.t(), "bias": bias_d}, ["y"])
+            outs.append(host(out["y"]))
+        img, _ = ctx.launch_log[-1]
+        assert ctx.poll() == 0
+    finally:
+        ctx.close()
+    tk = struct.unpack_from("<I", img, 48 + 24 + 16 + 8)[0]
+    assert tk < 4096, "expected a K-split plan"
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    check_bf16(outs[0], oracle_mm(a, wt, bias))
 
 
 def test_matmul_identity_and_zero_are_exact():

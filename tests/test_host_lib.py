@@ -232,6 +232,25 @@ def test_validator_rejects_corrupted_images():
         assert D.dvm_validate(b) == -5
 
 
+def test_validator_checks_the_matmul_k_split():
+    """A MatMul tile's third extent is its K-extent: 64-aligned, the tile count covers the
+    splits, and a split needs its partial tiles to fit the workspace."""
+    (img, _), = cxx_replay(W.MATMUL_ABS_OPS, {"A": ("bf16", (1, 4096), None),
+                                              "W": ("bf16", (4096, 4096), [1, 4096]),
+                                              "bias": ("bf16", (4096,), None)}, W.MATMUL_ABS_OUT)
+    assert D.dvm_validate(img) == 0
+    tk = struct.unpack_from("<I", img, 48 + 24 + 16 + 8)[0]
+    bd = struct.unpack_from("<I", img, 48)[0]
+    assert tk < 4096 and bd == 16 * (4096 // tk)
+    bad = [
+        _corrupt(img, 48 + 24 + 16 + 8, tk + 32, "<I"),     # t_K not a multiple of 64
+        _corrupt(img, 48 + 24 + 16 + 8, 2 * tk, "<I"),      # tile count no longer matches
+        _corrupt(img, 48 + 24 + 16 + 8, 64, "<I"),          # 64 splits: counts mismatch too
+    ]
+    for b in bad:
+        assert D.dvm_validate(b) == -5
+
+
 def test_encode_latency_is_microseconds():
     """In-library host time per LayerNorm instance (graph_add x9 + flush + encode)."""
     ctx = D.dvm_create_host()

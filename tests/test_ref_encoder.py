@@ -272,5 +272,25 @@ def test_cube_ring_stages(m):
     assert h["stage_bytes"] == (a_rows + tn) * 128 and h["stage_bytes"] % 1024 == 0
     assert h["n_stages"] == min(32, 196608 // h["stage_bytes"])
     assert 2 <= h["n_stages"] and h["n_stages"] * h["stage_bytes"] <= 196608
-    if m <= 8:
-        assert h["n_stages"] == 32   # small instances keep 32 k-blocks in flight
+
+
+@pytest.mark.parametrize("m,split", [(1, True), (64, True), (128, True), (129, False), (300, False), (8192, False)])
+def test_cube_k_split_plan(m, split):
+    """Few-row MatMuls split K across tiles wider than the unsplit plan's (the MMA thread's
+    per-k-block cost makes narrow tiles slow); large M keeps whole-K tiles.  Every plan
+    fills at most one wave and its partial tiles fit the workspace; instances of more than
+    one row tile never split."""
+    l, p = _counts(W.MATMUL_ABS_OPS, {"A": ("bf16", (m, 4096)), "W": ("bf16", (4096, 4096)),
+                                      "bias": ("bf16", (4096,))}, W.MATMUL_ABS_OUT,
+                   strides={"W": [1, 4096]})
+    pr = p[0][0]
+    tn, tk = pr["t"][1], pr["t"][2]
+    ks = -(-4096 // tk)
+    tiles_mn = -(-m // 128) * -(-4096 // tn)
+    assert tk % 64 == 0 and pr["block_dim"] == tiles_mn * ks
+    assert (ks > 1) == split
+    if split:
+        assert tn >= 64 and pr["block_dim"] <= 152
+        assert ks * tiles_mn * 128 * tn * 4 <= R.CUBE_WS_BYTES and tiles_mn <= R.CUBE_WS_TILES
+    else:
+        assert tk == 4096
