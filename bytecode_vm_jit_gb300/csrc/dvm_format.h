@@ -94,8 +94,8 @@ struct ProgRec {           // 64 bytes
   uint32_t body_off;       // byte offset of the body in the image
   uint32_t body_len;       // instructions
   uint32_t tens_off;       // byte offset of the tensor table
-  uint32_t n[4];
-  uint32_t t[4];
+  uint32_t n[4];            // iteration extents (MatMul: M, N)
+  uint32_t t[4];            // tile extents (MatMul: 128, t_N, t_K; block_dim counts K-splits)
   uint32_t K;
   uint32_t hoist_base;
 };

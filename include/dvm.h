@@ -27,7 +27,8 @@
  *   - A dvm_ctx is not thread-safe; use one per host thread.
  *   - Device memory is always owned by the caller (e.g. a torch tensor's data_ptr()).
  *     The context owns its graph state and a small device scratch area (grid-barrier
- *     counter and per-CTA partial sums) allocated by dvm_create.
+ *     counter and per-CTA partial sums) allocated by dvm_create, and the K-split MatMul
+ *     workspace allocated by its first K-split launch (see dvm_run).
  *   - Shapes are int64 extents, row-major; strides are in elements.
  *   - There is no CPU fallback: every op of the path runs in this library's kernels.
  */
@@ -176,11 +177,18 @@ dvm_status dvm_validate(const uint8_t* image, size_t len);
 /* Launch the interpreter for one image on `stream` (a cudaStream_t; NULL = legacy
  * default stream). tensor_ptrs are device pointers in binding order, each 16-byte
  * aligned. The image is copied into the kernel parameters, so `image` may be reused
- * as soon as the call returns. Asynchronous. */
+ * as soon as the call returns. Asynchronous.
+ * A MatMul image whose tile splits K (t_K < K; the tiler does this for instances of at
+ * most 128 rows) keeps fp32 partial tiles and per-tile arrival counters in a 32 MiB
+ * workspace of the context, allocated by the context's first such launch (that call
+ * then also allocates; DVM_E_CUDA if it cannot).  Like the grid-barrier scratch, the
+ * workspace is used by one launch at a time: launches of one context go on one stream,
+ * or are otherwise ordered. */
 dvm_status dvm_run(dvm_ctx* ctx, const uint8_t* image, size_t len, void* const* tensor_ptrs,
                    int n_tensors, void* stream);
 /* Synchronise `stream` and read the device status word (0 or a DVM_E_* device code).
- * A non-zero word is cleared and the grid-barrier state is re-initialised. */
+ * A non-zero word is cleared and the grid-barrier state and the K-split counters are
+ * re-initialised. */
 dvm_status dvm_poll_status(dvm_ctx* ctx, void* stream, int32_t* device_status);
 const char* dvm_last_error(const dvm_ctx* ctx);
 dvm_status dvm_stats(const dvm_ctx* ctx, dvm_stats_t* out);
