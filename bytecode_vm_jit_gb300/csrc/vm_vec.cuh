@@ -630,6 +630,11 @@ __device__ __forceinline__ void lds_vectors(float (&dst)[REG], const uint8_t* re
                                             const Lanes<VE>& L) {
   if (L.ur) {  // one row: the vectors sit at constant offsets from the first one
     const uint8_t* p = region + (size_t)(L.row0 * rstride + L.col0) * ESZ;
+    if (L.seg == (1u << Lanes<VE>::NV) - 1u) {
+#pragma unroll
+      for (int v = 0; v < Lanes<VE>::NV; v++) unpack<VE, ESZ>(p + v * (VE * 32 * ESZ), dst + v * VE);
+      return;
+    }
 #pragma unroll
     for (int v = 0; v < Lanes<VE>::NV; v++)
       if ((L.seg >> v) & 1u) unpack<VE, ESZ>(p + v * (VE * 32 * ESZ), dst + v * VE);
@@ -694,6 +699,11 @@ __device__ __forceinline__ void stg_vectors_fast(const float (&acc)[REG], uint8_
   const uint64_t pol = policy_stream();
   if (L.ur) {
     uint8_t* p = base + ((int64_t)(O.od[0] + L.row0) * vs0 + oin + L.col0) * ESZ;
+    if (L.seg == (1u << Lanes<VE>::NV) - 1u) {
+#pragma unroll
+      for (int v = 0; v < Lanes<VE>::NV; v++) pack_store<VE, ESZ>(p + v * (VE * 32 * ESZ), acc + v * VE, pol);
+      return;
+    }
 #pragma unroll
     for (int v = 0; v < Lanes<VE>::NV; v++)
       if ((L.seg >> v) & 1u) pack_store<VE, ESZ>(p + v * (VE * 32 * ESZ), acc + v * VE, pol);
@@ -1706,7 +1716,12 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         float* red = red_buf(rbuf);
         rbuf ^= 1;
         float s0 = ident, s1 = ident;
-        if (full) {
+        if (full && !mx && L.seg == (1u << NV) - 1u) {
+          // every vector present: s0 sums the even and s1 the odd values, in order, as one
+          // packed add per pair
+#pragma unroll
+          for (int e = 0; e < REG; e += 2) pair_op<OP_ADD>(s0, s1, s0, s1, A[e], A[e + 1]);
+        } else if (full) {
 #pragma unroll
           for (int v = 0; v < NV; v++) {
             if (!((L.seg >> v) & 1u)) continue;
