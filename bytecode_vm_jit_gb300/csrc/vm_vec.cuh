@@ -33,6 +33,8 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "dvm_internal.h"
 #include "vm_common.cuh"
 
@@ -1708,15 +1710,18 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
       // -------------------------------------------------------------- reductions
       case H_RSUM_U:
       case H_RMAX_U: {
+        // the max/sum choice is a compile-time constant inside: one code path per kind,
+        // no select per value
+        auto rred = [&](auto MXC) {
         // ACC (FULL) -> ACC (ROW), one tile row per thread.  Fixed order: the thread's
         // vectors in order (two interleaved partial sums), the warp butterfly, then
         // the partials of the row's warps in warp order; then the folded ROW ops.
-        const bool mx = u.h == H_RMAX_U;
+        constexpr bool mx = decltype(MXC)::value;
         const float ident = mx ? -INFINITY : 0.f;
         float* red = red_buf(rbuf);
         rbuf ^= 1;
         float s0 = ident, s1 = ident;
-        if (full && !mx && L.seg == (1u << NV) - 1u) {
+        if (!mx && full && L.seg == (1u << NV) - 1u) {
           // every vector present: s0 sums the even and s1 the odd values, in order, as one
           // packed add per pair
 #pragma unroll
@@ -1778,11 +1783,15 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
           else bin_vf_<VE, OP_SUB, false>(A, av, X);
           pc++;
         }
+        };
+        if (u.h == H_RMAX_U) rred(std::true_type{});
+        else rred(std::false_type{});
         break;
       }
       case H_RRED_G: {
+        auto rred = [&](auto MXC) {
         // general: one butterfly per segment, then each row's segments in order
-        const bool mx = u.op == OP_RMAX;
+        constexpr bool mx = decltype(MXC)::value;
         const float ident = mx ? -INFINITY : 0.f;
         float* red = red_buf(rbuf);
         rbuf ^= 1;
@@ -1811,6 +1820,9 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
           Q0[v] = q;
         }
         __syncwarp();
+        };
+        if (u.op == OP_RMAX) rred(std::true_type{});
+        else rred(std::false_type{});
         break;
       }
       case H_ASUM:
