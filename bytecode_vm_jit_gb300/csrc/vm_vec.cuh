@@ -1826,6 +1826,15 @@ __device__ __forceinline__ void exec_tile(const LaunchParams& Pm, const Prog& P,
         break;
       }
       case H_ASUM:
+        if (full && L.rowok == (1u << NV) - 1u) {
+          // a complete tile: even and odd values summed as packed pairs, in order, then
+          // the pair's total into the thread's running sum
+          float g0 = 0.f, g1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < REG; e += 2) pair_op<OP_ADD>(g0, g1, g0, g1, A[e], A[e + 1]);
+          grand += g0 + g1;
+          break;
+        }
 #pragma unroll
         for (int v = 0; v < NV; v++)
           if ((L.rowok >> v) & 1u) {
