@@ -255,3 +255,28 @@ def test_softmax_like_chain_rank3_ragged():
     ref = evaluate(ops, inp)
     check_f32(got["o"], ref["o"], 1e-5)
     check_f32(got["s"], ref["s"], 1e-5)
+
+
+@pytest.mark.parametrize("rows,dt,d", [(37, "f32", 4096), (64, "f32", 4096), (45, "bf16", 8192)])
+def test_softmax_rows_full_tiles(rows, dt, d):
+    """Row max and row sum over complete one-row tiles (the packed and compile-time paths
+    of the reduction handlers), a ragged last tile, and rows whose values are all
+    negative (the max starts from -inf, not from 0)."""
+    rng = np.random.default_rng(rows + d)
+    x = (rng.standard_normal((rows, d)) * 3.0).astype(np.float32)
+    x[1] = -np.abs(x[1]) - 5.0
+    x[rows - 1] = -np.abs(x[rows - 1]) - 50.0
+    if dt == "bf16":
+        xb = W.f32_to_bf16_bits(x)
+        inp = {"x": (xb, "bf16")}
+    else:
+        inp = {"x": (x, "f32")}
+    ops = [("reduce_max", ["x"], "m", "f32", ()), ("sub", ["x", "m"], "z", "f32", ()),
+           ("exp", ["z"], "e", "f32", ()), ("reduce_sum", ["e"], "s", "f32", ()),
+           ("div", ["e", "s"], "p", "f32", ())]
+    got = run(ops, inp, ["p", "m", "s"])
+    ref = evaluate(ops, inp)
+    check_f32(got["m"], ref["m"], 1e-6)
+    check_f32(got["s"], ref["s"], 1e-5)
+    check_f32(got["p"], ref["p"], 1e-5)
+    assert np.all(got["m"][1] < 0) and np.all(got["m"][rows - 1] < -40)
