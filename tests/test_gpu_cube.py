@@ -233,8 +233,10 @@ def test_addmm(m):
     check_bf16(got, ref)
 
 
-@pytest.mark.parametrize("m,out_dt", [(1, "bf16"), (300, "bf16"), (129, "f32"), (1000, "f32")])
+@pytest.mark.parametrize("m,out_dt", [(1, "bf16"), (300, "bf16"), (129, "f32"), (1000, "f32"), (1, "f32"), (64, "f32")])
 def test_matmul_alone(m, out_dt):
+    """The MatMul op with no epilogue ops, bf16 or fp32 result; M = 1 and 64 run as
+    K-split tiles (fp32 partials summed in split order), within the same fp32 bound."""
     wt, _, _ = W.matmul_params()
     inp = W.matmul_inputs(m + 1000, m, small_params=(wt, np.zeros(W.MM_N, np.uint16)))
     ops = [("matmul", ["A", "W"], "y", out_dt, ())]
