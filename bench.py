@@ -675,8 +675,10 @@ def e2e_layernorm(wl, run, stream, sptr, n_copy=1):
     upload stream, the launch waits for it, and y comes back on a download stream once
     its launch is done, so uploads, launches and downloads of neighbouring instances
     overlap (one stream per direction measured fastest; `n_copy` splits each copy into
-    chunks on that many streams).  An upload into a pool region waits for the launch two
-    instances back (the rotating pools reuse a region only after several instances)."""
+    chunks on that many streams).  The device pools rotate, so a region is reused after
+    several instances: an upload waits for the last earlier launch that read an
+    overlapping x region, and a launch waits for the last earlier download that read an
+    overlapping y region (no fixed pipeline depth, no write over data still in use)."""
     import torch
     max_r = max(wl.sizes)
     hx = torch.empty(max_r * wl.d, dtype=torch.float32, pin_memory=True)
@@ -685,20 +687,36 @@ def e2e_layernorm(wl, run, stream, sptr, n_copy=1):
     up = [torch.cuda.Stream() for _ in range(n_copy)]
     down = [torch.cuda.Stream() for _ in range(n_copy)]
     insts = [wl.instance(i) for i in range(len(wl.sizes))]
+
+    def region(t):
+        return t.data_ptr(), t.numel() * t.element_size()
+
+    def last_overlap(regs, i):
+        a, n = regs[i]
+        for j in range(i - 1, -1, -1):
+            b, m = regs[j]
+            if a < b + m and b < a + n:
+                return j
+        return -1
+
+    xr = [region(ins["x"]) for _, ins, _ in insts]
+    yr = [region(outs["y"]) for _, _, outs in insts]
+    x_dep = [last_overlap(xr, i) for i in range(len(insts))]
+    y_dep = [last_overlap(yr, i) for i in range(len(insts))]
     h2d = d2h = 0
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    done = []
+    done, dl_done = [], []
     for i, (ops, ins, outs) in enumerate(insts):
         n = ins["x"].numel()
         bounds = [n * c // n_copy for c in range(n_copy + 1)]
         ups = []
         for c, st in enumerate(up):
             st.wait_event(e0)
-            if i >= 2:
-                st.wait_event(done[i - 2])
+            if x_dep[i] >= 0:
+                st.wait_event(done[x_dep[i]])
             with torch.cuda.stream(st):
                 ins["x"].view(-1)[bounds[c]:bounds[c + 1]].copy_(hx[bounds[c]:bounds[c + 1]], non_blocking=True)
                 ev = torch.cuda.Event()
@@ -706,15 +724,23 @@ def e2e_layernorm(wl, run, stream, sptr, n_copy=1):
                 ups.append(ev)
         for ev in ups:
             stream.wait_event(ev)
+        if y_dep[i] >= 0:
+            for ev in dl_done[y_dep[i]]:
+                stream.wait_event(ev)
         h2d += n * 4
         run.feed(ops, ins, outs, sptr)
         k = torch.cuda.Event()
         k.record(stream)
         done.append(k)
+        dls = []
         for c, st in enumerate(down):
             st.wait_event(k)
             with torch.cuda.stream(st):
                 hy[bounds[c]:bounds[c + 1]].copy_(outs["y"].view(-1)[bounds[c]:bounds[c + 1]], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(st)
+                dls.append(ev)
+        dl_done.append(dls)
         d2h += n * 4
     for st in down + up:
         stream.wait_stream(st)
