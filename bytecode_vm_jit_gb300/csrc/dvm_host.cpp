@@ -761,11 +761,6 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
     if (rows * cand[r - 1] > D.cap_elems) return;
     int64_t tiles[4] = {1, 1, 1, 1};
     for (int d = 0; d < r; d++) tiles[d] = cdiv(n[d], cand[d]);
-    int64_t rws;
-    flags_for(p, cand, tiles, li, &rws);
-    int64_t stage, hoist;
-    layout(p, li, &stage, &hoist, nullptr, nullptr);
-    if (2 * stage + hoist > D.smem_budget) return;
     int64_t ntiles = 1;
     for (int d = 0; d < r; d++) ntiles *= tiles[d];
     int64_t waves = cdiv(ntiles, D.num_cores);
@@ -778,6 +773,14 @@ void plan_vec(const dvm_ctx* c, Program& p, bool rowred) {
     }
     int64_t cost = waves * (D.c0_bytes + tb);
     const int mis = warp_aligned(cand) ? 0 : 1;
+    // a candidate that cannot beat the best so far is not laid out at all (the feasibility
+    // test below only matters for a winner): the same choice, less work per instance
+    if (have && (mis > best_mis || (mis == best_mis && cost >= best_cost))) return;
+    int64_t rws;
+    flags_for(p, cand, tiles, li, &rws);
+    int64_t stage, hoist;
+    layout(p, li, &stage, &hoist, nullptr, nullptr);
+    if (2 * stage + hoist > D.smem_budget) return;
     if (!have || mis < best_mis || (mis == best_mis && cost < best_cost)) {
       have = true;
       best_cost = cost;
