@@ -28,6 +28,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 using namespace dvm;
@@ -215,6 +216,14 @@ struct dvm_ctx {
   std::vector<int8_t> slot_of;
   std::vector<int8_t> kind_of;  // 0 unknown, 1 FULL, 2 ROW
   std::vector<uint8_t> in_group;
+  // static-graph fusion: whether a group, grown by one more op, still lowers (the dry run)
+  // depends only on the op stream's structure (op codes, wiring, dtypes, output marks,
+  // ranks, unit extents and stride patterns), not on the extents themselves.  `sig` is a
+  // running hash of that structure since the last reset; `fuse_memo` keeps the dry run's
+  // verdict per stream prefix across instances, so a repeated op stream (every instance
+  // of a dynamic-shape workload) lowers each candidate group only the first time.
+  uint64_t sig = 0;
+  std::unordered_map<uint64_t, bool> fuse_memo;
 
   int fail(int code, const char* fmt, const char* a = "") {
     std::snprintf(err, sizeof err, fmt, a);
@@ -235,6 +244,29 @@ struct Timer {
     c->stats.host_ns_last += ns;
   }
 };
+
+// 64-bit mixing of the stream signature (the finaliser of MurmurHash3)
+inline uint64_t mix64(uint64_t h, uint64_t x) {
+  h ^= x + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+  h ^= h >> 33;
+  h *= 0xff51afd7ed558ccdull;
+  h ^= h >> 33;
+  h *= 0xc4ceb9fe1a85ec53ull;
+  h ^= h >> 33;
+  return h;
+}
+// structural class of a value: dtype, rank, and per dim whether the extent is 1 and
+// whether the stride is 0, contiguous or other
+uint64_t shape_class(const Value& v) {
+  uint64_t k = (uint64_t)v.shape.rank | ((uint64_t)(uint8_t)v.dtype << 4);
+  int64_t cs = 1;
+  for (int d = v.shape.rank - 1; d >= 0; d--) {
+    const uint64_t st = v.strides[d] == 0 ? 0 : (v.strides[d] == cs ? 1 : 2);
+    k |= ((v.shape.d[d] == 1 ? 1ull : 0ull) | (st << 1)) << (8 + 3 * d);
+    cs *= v.shape.d[d];
+  }
+  return k;
+}
 
 Shape iter_shape(const dvm_ctx* c, const Op& op) {
   if (op.cls == C_RRED || op.cls == C_ARED) return c->values[op.in[0]].shape;
@@ -555,7 +587,7 @@ bool dry_run(dvm_ctx* c, const Group& g, int32_t extra) {
   return true;
 }
 
-bool accepts(dvm_ctx* c, int32_t gi, int32_t oi) {
+bool accepts(dvm_ctx* c, int32_t gi, int32_t oi, uint64_t key) {
   Group& g = c->groups[gi];
   const Op& op = c->ops[oi];
   Shape isG = iter_shape(c, op);
@@ -601,7 +633,12 @@ bool accepts(dvm_ctx* c, int32_t gi, int32_t oi) {
       return false;
     }
   }
-  return dry_run(c, g, oi);
+  auto it = c->fuse_memo.find(key);
+  if (it != c->fuse_memo.end()) return it->second;
+  const bool ok = dry_run(c, g, oi);
+  if (c->fuse_memo.size() >= 8192) c->fuse_memo.clear();
+  c->fuse_memo.emplace(key, ok);
+  return ok;
 }
 
 void append(dvm_ctx* c, int32_t gi, int32_t oi) {
@@ -1255,6 +1292,7 @@ dvm_status dvm_reset(dvm_ctx* c) {
   c->plan_valid.assign(c->plan_valid.size(), 0);
   c->open = -1;
   c->stats.host_ns_last = 0;
+  c->sig = 0;
   return DVM_OK;
 }
 
@@ -1287,6 +1325,7 @@ dvm_status dvm_input(dvm_ctx* c, dvm_dtype dtype, int rank, const int64_t* shape
   }
   c->values.push_back(v);
   *out_id = (int32_t)c->values.size() - 1;
+  c->sig = mix64(c->sig, 0x100000000ull ^ shape_class(v));
   return DVM_OK;
 }
 
@@ -1303,6 +1342,7 @@ dvm_status dvm_graph_add(dvm_ctx* c, dvm_op opc, const int32_t* inputs, int n_in
   if (!infer && (rank < 0 || rank > 4 || (rank > 0 && !shape))) return c->fail(DVM_E_INVALID_ARG, "bad rank");
   c->stats.ops_added++;
   if (cls == C_OPQ) {
+    c->sig = mix64(c->sig, 0x300000000ull);
     close_open(c);
     if (rank == 0) {
       *out_id = -1;
@@ -1375,10 +1415,17 @@ dvm_status dvm_graph_add(dvm_ctx* c, dvm_op opc, const int32_t* inputs, int n_in
   op.shape = sh;
   c->ops.push_back(op);
   int32_t oi = (int32_t)c->ops.size() - 1;
+  // the stream signature with this op: code, dtype, wiring and structural shape classes
+  uint64_t key = mix64(c->sig, (uint64_t)code | ((uint64_t)out_dtype << 16) | ((uint64_t)need << 24) |
+                                   ((uint64_t)op.n_attrs << 28) | 0x400000000ull);
+  for (int i = 0; i < need; i++)
+    key = mix64(key, ((uint64_t)(uint32_t)inputs[i] << 32) ^ shape_class(c->values[inputs[i]]));
+  key = mix64(key, shape_class(c->values[vid]));
+  c->sig = key;
   if (cls == C_MM) {
     close_open(c);
     start_group(c, PK_CUBE, sh, oi);
-  } else if (c->open >= 0 && accepts(c, c->open, oi)) {
+  } else if (c->open >= 0 && accepts(c, c->open, oi, key)) {
     append(c, c->open, oi);
   } else {
     Shape G = iter_shape(c, c->ops[oi]);
@@ -1421,6 +1468,7 @@ dvm_status dvm_graph_add_n(dvm_ctx* c, const dvm_op_desc* ops, int n, int32_t* o
 dvm_status dvm_mark_output(dvm_ctx* c, int32_t id) {
   if (!c || id < 0 || id >= (int32_t)c->values.size()) return DVM_E_INVALID_ARG;
   c->values[id].output = true;
+  c->sig = mix64(c->sig, 0x200000000ull ^ (uint64_t)id);
   for (size_t i = 0; i < c->plan_valid.size(); i++) c->plan_valid[i] = 0;
   return DVM_OK;
 }

@@ -31,9 +31,14 @@ def test_library_exports_every_declared_symbol():
     assert set(declared) == set(D.EXPORTS)
 
 
-def cxx_replay(ops, inputs, outputs, desc=None):
-    """Feed an op list through the C++ library (encode-only context)."""
-    ctx = D.dvm_create_host(**(desc or {}))
+def cxx_replay(ops, inputs, outputs, desc=None, ctx=None):
+    """Feed an op list through the C++ library (encode-only context; a given context is
+    reset and reused, keeping what it has learnt about earlier op streams)."""
+    own = ctx is None
+    if own:
+        ctx = D.dvm_create_host(**(desc or {}))
+    else:
+        D.dvm_reset(ctx)
     ids = {}
     out = []
     try:
@@ -55,7 +60,8 @@ def cxx_replay(ops, inputs, outputs, desc=None):
                 D.dvm_mark_output(ctx, ids[name])
         flush()
     finally:
-        D.dvm_destroy(ctx)
+        if own:
+            D.dvm_destroy(ctx)
     return out
 
 
@@ -336,3 +342,36 @@ def test_op_batch_splits_at_opaque_ops():
     assert [opq for _, _, _, opq in b.packed] == [True, False]
     assert b.ids == {"x": 0, "a": 1, "b": 2, "c": 3}
     assert [list(e) for _, e, _, _ in b.packed] == [[1, -1], [2, 3]]
+
+
+def test_fusion_memo_across_op_streams():
+    """The fuser keeps its fusion verdicts per op-stream structure across resets: one
+    context fed a mix of streams (same ops with one row and many, strided inputs, a chain
+    whose group must be split, then the first stream again) encodes every one of them to
+    the same bytes as a fresh context does."""
+    chain = [("adds", ["x"], "t1", "f32", (1.0, 0)), ("muls", ["x"], "t2", "f32", (2.0, 0)),
+             ("muls", ["x"], "t3", "f32", (3.0, 0)), ("add", ["t1", "t2"], "t4", "f32", ()),
+             ("add", ["t4", "t3"], "t5", "f32", ()), ("mul", ["t5", "t1"], "t6", "f32", ()),
+             ("add", ["t6", "t2"], "y", "f32", ())]
+    streams = [
+        (W.LAYERNORM_OPS, ln_inputs(8192), W.LAYERNORM_OUT),
+        (W.LAYERNORM_OPS, ln_inputs(1), W.LAYERNORM_OUT),
+        (W.LAYERNORM_OPS, ln_inputs(300), W.LAYERNORM_OUT),
+        (W.SQRT_ADD_OPS, {"a": ("f32", (64, 1024), [2048, 1]), "b": ("f32", (64, 1024), None)}, W.SQRT_ADD_OUT),
+        (W.SQRT_ADD_OPS, {"a": ("f32", (64, 1024), None), "b": ("f32", (64, 1024), None)}, W.SQRT_ADD_OUT),
+        (chain, {"x": ("f32", (100, 512), None)}, ["y", "t3"]),
+        (chain, {"x": ("f32", (100, 512), None)}, ["y"]),
+        (W.IF_ELSE_ADD_OPS, {"x": ("bf16", (300, 8192), None), "z": ("bf16", (300, 8192), None)}, W.IF_ELSE_ADD_OUT),
+        (W.LAYERNORM_OPS, ln_inputs(8192), W.LAYERNORM_OUT),
+        (W.LAYERNORM_OPS, ln_inputs(1), W.LAYERNORM_OUT),
+    ]
+    shared = D.dvm_create_host()
+    try:
+        for rep in range(2):
+            for ops, inputs, outs in streams:
+                got = cxx_replay(ops, inputs, outs, ctx=shared)
+                want = cxx_replay(ops, inputs, outs)
+                assert [img for img, _ in got] == [img for img, _ in want]
+                assert [b for _, b in got] == [b for _, b in want]
+    finally:
+        D.dvm_destroy(shared)
